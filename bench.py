@@ -1,0 +1,400 @@
+"""Benchmark: INT4 decode block-step on GB300.
+
+Default workload: one Llama-3.1-8B-shaped decoder block (hidden 4096, 32/8
+heads, head_dim 128, SwiGLU 14336), batch 1, 1024 cached positions in the INT4
+rotated KV cache.  A step is one futr_decode_block call (QKV + RoPE + rotation
++ INT4 KV append, attention, O + residual, gate/up + SwiGLU, down + residual).
+
+Timing: the K timed steps are one CUDA-graph replay (5 kernels per step,
+programmatic dependent launch between them), bracketed by CUDA events on the
+capturing stream; steps cycle over distinct copies of the layer (weights and
+cache) totalling more than 4x the L2, so every step streams from HBM.  One
+JSON line on stdout (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl futr|reference]
+
+--impl reference times the float64 CPU oracle on the host cores instead.
+Under torchrun (N > 1) every rank runs an independent replica (no collective
+on the data path); elapsed time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from int4_weight_kv_w4a16_gb300 import inputs  # noqa: E402
+
+METRIC = "INT4 decode µs/block-step (8B/70B, batch 1–32); achieved HBM TB/s vs peak"
+UNIT = "us/block-step"
+N_LAYERS_MODEL = {4096: 32, 8192: 80}
+
+
+# ------------------------------------------------------------- byte model --
+
+def proj_bytes(rows: int, cols: int) -> int:
+    """INT4 codes + fp16 group-128 scales of one projection."""
+    return rows * cols // 2 + rows * (cols // 128) * 2
+
+
+def stage_bytes(shape, lengths) -> dict:
+    """Algorithmic HBM bytes of each kernel of one block-step: weights, KV
+    codes + scales read (new token included) and written, activations read
+    and written once."""
+    b = len(lengths)
+    H, I, Hq, Hkv, d = shape.hidden, shape.inter, shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    kv_tok = Hkv * (d + 4)
+    kv_read = int(sum(int(L) + 1 for L in lengths)) * kv_tok
+    qd = Hq * d
+    return {
+        "qkv": proj_bytes(shape.qkv_rows, H) + b * H * 2 + b * qd * 2 + b * kv_tok,
+        "attention": b * qd * 2 + kv_read + b * qd * 2,
+        "o": proj_bytes(H, qd) + b * qd * 2 + b * H * 2 + b * H * 2,
+        "gate_up": proj_bytes(2 * I, H) + b * H * 2 + b * I * 2,
+        "down": proj_bytes(H, I) + b * I * 2 + b * H * 2 + b * H * 2,
+    }
+
+
+STAGES = ["qkv", "attention", "o", "gate_up", "down"]
+
+
+# ------------------------------------------------------------------ peaks --
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(", ") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------- distributed glue --
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a float over the process group (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------- CPU baseline --
+
+def oracle_baseline(wl, budget_s: float = 15.0, max_steps: int = 20, min_steps: int = 1):
+    """Time the float64 oracle's decode_block on the host cores, on the same
+    workload, for a bounded number of block-steps."""
+    import oracle
+    shape = wl.shape
+    lengths = inputs.context_lengths(wl)
+    w = inputs.block_weights(shape, 0)
+    wdq = oracle.dequant_block(oracle.pack_block(w))
+    del w
+    x = inputs.activations(shape, wl.batch, 0)
+    hist = inputs.kv_history(shape, lengths, n_outlier=wl.n_outlier, seed=0)
+    cache = oracle.build_cache(hist, shape)
+    del hist
+    pos = np.asarray(lengths)
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_steps and (len(times) < min_steps or time.perf_counter() - t_all < budget_s):
+        t0 = time.perf_counter()
+        oracle.decode_block(x, wdq, cache, pos, shape)
+        times.append(time.perf_counter() - t0)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": 1e6 * statistics.mean(times), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} full block-steps of {wl.name} (float64 numpy, weights pre-dequantized "
+                      f"outside the timed region)"}
+
+
+# ------------------------------------------------------------- GPU bench --
+
+class Bench:
+    def __init__(self, wl, device: int):
+        import torch
+        from int4_weight_kv_w4a16_gb300 import build, futr
+        build.build()
+        self.torch, self.futr = torch, futr
+        torch.cuda.set_device(device)
+        self.wl, self.shape = wl, wl.shape
+        self.cs = futr.make_shape(self.shape)
+        self.lengths = inputs.context_lengths(wl)
+        self.b = wl.batch
+        self.cap = int(max(self.lengths)) + 16
+        blob_bytes = futr.futr_weights_size(self.cs)
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.n_copies = max(2, math.ceil(4 * l2 / blob_bytes))
+        w = inputs.block_weights(self.shape, 0)
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.blobs = [futr.alloc_bytes(blob_bytes) for _ in range(self.n_copies)]
+        wd = {k: dev(v) for k, v in w.items()}
+        futr.futr_pack_weights(self.cs, wd["wq"], wd["wk"], wd["wv"], wd["wo"], wd["wgate"], wd["wup"],
+                               wd["wdown"], wd["g_attn"], wd["g_mlp"], self.blobs[0])
+        del wd, w
+        for bl in self.blobs[1:]:
+            bl.copy_(self.blobs[0])
+        self.kv = futr.futr_kv_init(self.cs, self.n_copies, self.b, self.cap,
+                                    futr.alloc_bytes(futr.futr_kv_size(self.cs, self.n_copies, self.b, self.cap)))
+        self.ws = futr.futr_workspace_init(self.cs, self.b, self.cap,
+                                           futr.alloc_bytes(futr.futr_workspace_size(self.cs, self.b, self.cap)))
+        hist = inputs.kv_history(self.shape, self.lengths, n_outlier=wl.n_outlier, seed=0)
+        for layer in range(self.n_copies):
+            for s, (kb, vb) in enumerate(hist):
+                futr.futr_kv_append(self.kv, layer, s, 1, dev(np.array([0], np.int32)), kb.shape[1], dev(kb), dev(vb))
+        del hist
+        self.x = dev(inputs.activations(self.shape, self.b, 0).view(np.int16))
+        self.pos = dev(np.asarray(self.lengths, np.int32))
+        self.y = torch.empty_like(self.x)
+        torch.cuda.synchronize()
+        st = futr.futr_check(self.ws, self.kv)
+        if st != 0:
+            raise RuntimeError(futr.futr_status_string(st))
+        self.bytes = stage_bytes(self.shape, self.lengths)
+        self.blob_bytes = blob_bytes
+
+    def step(self, k: int):
+        layer = k % self.n_copies
+        self.futr.futr_decode_block(self.x, self.blobs[layer], self.kv, layer, self.b, self.pos, self.y, self.ws)
+
+    def timed(self, steps: int, warmup: int):
+        torch = self.torch
+        for k in range(warmup):
+            self.step(k)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                for k in range(steps):
+                    self.step(k)
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()  # untimed: uploads the executable graph
+        torch.cuda.synchronize()
+        st = self.futr.futr_check(self.ws, self.kv)
+        if st != 0:
+            raise RuntimeError(self.futr.futr_status_string(st))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        return g, e0, e1
+
+    def stage_times(self, n: int):
+        acc = np.zeros(5)
+        for k in range(n):
+            layer = k % self.n_copies
+            acc += np.array(self.futr.futr_decode_block_timed(self.x, self.blobs[layer], self.kv, layer, self.b,
+                                                              self.pos, self.y, self.ws))
+        return acc / n
+
+    def e2e(self, n: int):
+        torch = self.torch
+        xh = self.x.cpu().pin_memory()
+        ph = self.pos.cpu().pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        for k in range(3):
+            self.futr.futr_decode_block_host(xh, self.blobs[k % self.n_copies], self.kv, k % self.n_copies, self.b,
+                                             ph, yh, self.ws)
+        t0 = time.perf_counter()
+        for k in range(n):
+            layer = k % self.n_copies
+            self.futr.futr_decode_block_host(xh, self.blobs[layer], self.kv, layer, self.b, ph, yh, self.ws)
+        dt = time.perf_counter() - t0
+        return {"value": 1e6 * dt / n, "unit": UNIT, "h2d_bytes_per_step": int(self.b * self.shape.hidden * 2 + self.b * 4),
+                "d2h_bytes_per_step": int(self.b * self.shape.hidden * 2)}
+
+
+def run_futr(args, wl):
+    rank, world, local = dist_env()
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    B = Bench(wl, local)
+    g, e0, e1 = B.timed(args.steps, args.warmup)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    st = B.futr.futr_check(B.ws, B.kv)
+    if st != 0:
+        raise RuntimeError(B.futr.futr_status_string(st))
+    ms = max_over_ranks(ms, world)
+    us_step = 1000.0 * ms / args.steps
+    value = us_step / world  # whole-job µs per block-step (replicas in parallel)
+    stage_ms = B.stage_times(min(args.steps, 30))
+    pk = peaks()
+    total_bytes = sum(B.bytes.values())
+    dom = int(np.argmax(stage_ms))
+    dom_name = STAGES[dom]
+    dom_gbs = B.bytes[dom_name] / (stage_ms[dom] * 1e-3) / 1e9
+    e2e = B.e2e(min(args.steps, 50))
+    sh = B.shape
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "hidden": sh.hidden, "n_q_heads": sh.n_q_heads, "n_kv_heads": sh.n_kv_heads,
+                   "head_dim": sh.head_dim, "inter": sh.inter, "batch": B.b,
+                   "ctx": "ragged %d-%d (mean %.0f)" % (wl.ragged[0], wl.ragged[1], np.mean(B.lengths))
+                   if wl.ragged else int(wl.ctx),
+                   "weights": "int4 group-128 fp16 scales", "kv_cache": "int4 Hadamard-rotated, fp16 scale per token-head",
+                   "l2": f"steps cycle {B.n_copies} distinct layer copies ({B.n_copies * B.blob_bytes / 1e6:.0f} MB of weights) "
+                         f"> 4x L2", "timing": "CUDA graph of K steps, 5 kernels/step, programmatic dependent launch",
+                   "parallelism": f"replicas x{world}"},
+        "block_roofline": {"bound": "hbm", "algorithmic_bytes": int(total_bytes),
+                           "achieved": round(total_bytes / (us_step * 1e-6) / 1e9, 1), "peak": pk["hbm_gbs"],
+                           "unit": "GB/s", "frac": round(total_bytes / (us_step * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+                           "peak_source": pk["source"]},
+        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(dom_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                     "algorithmic_bytes": int(B.bytes[dom_name]), "avg_launch_us": round(stage_ms[dom] * 1e3, 3),
+                     "peak_source": pk["source"]},
+        "stage_us": {n: round(float(t) * 1e3, 3) for n, t in zip(STAGES, stage_ms)},
+        "tokens_per_s_blocks_only": round(B.b / (us_step * 1e-6 * N_LAYERS_MODEL.get(sh.hidden, 32)), 1),
+        "e2e": e2e, "clocks": clk, "gpu_launches": 5 * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(wl)
+    if rank == 0:
+        out = json.dumps(line)
+        print(out, flush=True)
+        if args.out:
+            with open(args.out, "a") as f:
+                f.write(out + "\n")
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    import oracle
+    shape = wl.shape
+    lengths = inputs.context_lengths(wl)
+    w = inputs.block_weights(shape, 0)
+    wdq = oracle.dequant_block(oracle.pack_block(w))
+    del w
+    x = inputs.activations(shape, wl.batch, 0)
+    hist = inputs.kv_history(shape, lengths, n_outlier=wl.n_outlier, seed=0)
+    cache = oracle.build_cache(hist, shape)
+    pos = np.asarray(lengths)
+    for _ in range(args.warmup):
+        oracle.decode_block(x, wdq, cache, pos, shape)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_block(x, wdq, cache, pos, shape)
+    dt = time.perf_counter() - t0
+    us = 1e6 * dt / args.steps
+    line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1000, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.batch},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} full block-steps of {wl.name}, float64 numpy oracle"},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="llama8b_b1_ctx1024", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="futr", choices=["futr", "reference"])
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if args.steps > 20:
+            args.steps = 20  # bounded CPU sample
+        run_reference(args, wl)
+    else:
+        run_futr(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+/*
+ * futr.h -- C ABI of libfutr.so: the INT4-weight / INT4-KV decode step of a
+ * Llama-style Transformer block on GB300 (sm_103a).
+ *
+ * The operations follow "FuTransformer: FP8 prefill and INT4 decode for
+ * Llama-style inference on Hopper" (abstract) and its English explainer "FP8
+ * Prefill + INT4 Decode: New Optimization for Llama Inference on Hopper"
+ * (sections "FP8 Prefill: fusing GEMM and epilogue all the way" for the gain
+ * folding and direct KV-cache placement, "INT4 Decode: letting dequantization
+ * feed directly into MMA operands" for the INT4 projections and the INT4
+ * KV-cache copy, and the paragraph on the block-diagonal Hadamard transform).
+ *
+ * Conventions shared by every call
+ *  - Every buffer argument is a DEVICE pointer unless its name ends in _host.
+ *    All device buffers are owned by the caller; the library allocates no
+ *    device memory.  Buffers must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on that stream unless stated otherwise.
+ *  - Host-detectable errors (bad shapes, null pointers, sizes) are returned
+ *    immediately and nothing is launched.  Errors found on the device (a
+ *    position outside the cache, a bad blob header, a wait that ran out) set
+ *    an error word in the workspace; futr_check() returns it.  No kernel traps.
+ *  - bf16 and fp16 values are passed as uint16_t bit patterns.
+ *  - Supported shapes: head_dim 64 or 128; group 128; had_block a power of two
+ *    between 2 and head_dim; hidden, n_q_heads*head_dim, inter multiples of
+ *    128; n_q_heads a multiple of n_kv_heads with at most 16 query heads per
+ *    kv-head; batch 1..32; KV capacity up to 65536 positions per sequence.
+ */
+#ifndef FUTR_H_
+#define FUTR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t futr_status;
+#define FUTR_OK                0
+#define FUTR_ERR_INVALID_ARG   1  /* null pointer, size too small, index out of range */
+#define FUTR_ERR_UNSUPPORTED   2  /* shape or batch outside the supported set         */
+#define FUTR_ERR_CUDA          3  /* a CUDA runtime call failed                       */
+#define FUTR_ERR_OUT_OF_RANGE  4  /* device: pos[b] outside [0, capacity)             */
+#define FUTR_ERR_TIMEOUT       5  /* device: a bounded wait ran out                   */
+#define FUTR_ERR_BAD_BLOB      6  /* device or host: weight blob header mismatch      */
+
+/* Shape of one decoder block. */
+typedef struct futr_shape {
+  int32_t hidden;      /* model width H                                  */
+  int32_t n_q_heads;   /* query heads Hq                                 */
+  int32_t n_kv_heads;  /* key/value heads Hkv (grouped-query attention)  */
+  int32_t head_dim;    /* d                                              */
+  int32_t inter;       /* SwiGLU intermediate width I                    */
+  int32_t group;       /* INT4 scale group along the input dim (128)     */
+  int32_t had_block;   /* Hadamard block size along head_dim             */
+  float rms_eps;       /* RMSNorm epsilon (1e-5)                         */
+  float rope_theta;    /* RoPE base (500000)                             */
+} futr_shape;
+
+/* INT4 KV cache descriptor: plain data filled by futr_kv_init, kept by the
+ * caller (host memory).  `base` is the caller's device buffer. */
+typedef struct futr_kv {
+  futr_shape shape;
+  int32_t n_layers, max_batch, capacity;   /* capacity: positions per sequence */
+  int32_t _pad;
+  void* base;
+  uint64_t bytes;
+  uint64_t stream_bytes;                   /* bytes of one (layer, seq, kv-head) stream */
+  uint64_t rope_offset;                    /* cos/sin table [capacity][d/2] float2      */
+  uint64_t err_offset;                     /* int32 error word of futr_kv_append        */
+  uint64_t magic;
+} futr_kv;
+
+/* Workspace descriptor: plain data filled by futr_workspace_init.  The
+ * offsets name the intermediate activations of the last decode call. */
+typedef struct futr_ws {
+  futr_shape shape;
+  int32_t max_batch, capacity, n_sm, _pad;
+  void* base;
+  uint64_t bytes;
+  uint64_t off_err;      /* int32 error word                                   */
+  uint64_t off_qrot;     /* fp16 [b][Hq][d]   rotated query                     */
+  uint64_t off_o;        /* bf16 [b][Hq*d]    attention output (unrotated)      */
+  uint64_t off_h;        /* bf16 [b][H]       residual after attention          */
+  uint64_t off_a;        /* bf16 [b][I]       SwiGLU activation                 */
+  uint64_t off_xin;      /* bf16 [b][H]       staging for futr_decode_block_host */
+  uint64_t off_yout;     /* bf16 [b][H]                                          */
+  uint64_t off_pos;      /* int32 [b]                                            */
+  uint64_t off_part;     /* fp32 split-K partial sums                            */
+  uint64_t part_bytes;
+  uint64_t off_apart;    /* fp32 split-context attention partials                */
+  uint64_t apart_bytes;
+  uint64_t off_cnt;      /* uint32 arrival counters (self-resetting)             */
+  uint64_t cnt_words;
+  uint64_t magic;
+} futr_ws;
+
+/* Which projection a canonical (unpacked) view refers to. */
+#define FUTR_PROJ_QKV   0   /* rows: Wq; Wk; Wv  [Hq*d + 2*Hkv*d, H], gain g_attn */
+#define FUTR_PROJ_O     1   /* [H, Hq*d], no gain                                   */
+#define FUTR_PROJ_GATE  2   /* [I, H], gain g_mlp                                   */
+#define FUTR_PROJ_UP    3   /* [I, H], gain g_mlp                                   */
+#define FUTR_PROJ_DOWN  4   /* [H, I], no gain                                      */
+
+/* Human-readable text for a status code (static string). */
+const char* futr_status_string(futr_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t futr_version(void);
+
+/* Bytes of the packed weight blob of one block for `shape`. */
+futr_status futr_weights_size(const futr_shape* shape, size_t* bytes);
+
+/*
+ * Offline packer (abstract: "folding the fixed RMSNorm gain into weights";
+ * "INT4 projection weights", "round-to-nearest weights"; explainer, INT4 Decode
+ * section: weights "stored according to the Tensor Core fragment layout").
+ *
+ * Inputs are fp32 device matrices in nn.Linear layout [out, in], row-major:
+ * wq [Hq*d, H], wk/wv [Hkv*d, H], wo [H, Hq*d], wgate/wup [I, H], wdown [H, I],
+ * and the RMSNorm gains g_attn, g_mlp [H].  For every projection W' = W diag(g)
+ * (g_attn for q/k/v, g_mlp for gate/up, none for o/down) is rounded once to
+ * fp32, then each (output row, 128-input group) gets the fp16 scale
+ * s = fp16(max|W'| / 7) (fp32 division, nearest-even; saturates at 65504) and
+ * codes c = clamp(round_half_even(fp32(W' / s)), -8, 7) (all 0 when s == 0).
+ * The blob (`blob_bytes` >= futr_weights_size) receives a 256-byte header and
+ * four sections (QKV, O, gate/up interleaved per 64 rows, down) of 8448-byte
+ * units: 128 output rows x 128 inputs of nibbles in mma.m16n8k16 A-fragment
+ * order, then the units' 128 fp16 scales.
+ */
+futr_status futr_pack_weights(const futr_shape* shape,
+                              const float* wq, const float* wk, const float* wv,
+                              const float* wo, const float* wgate, const float* wup,
+                              const float* wdown, const float* g_attn, const float* g_mlp,
+                              void* blob, size_t blob_bytes, void* stream);
+
+/*
+ * Canonical view of one packed projection (for verification): codes int8
+ * [rows, cols] row-major in [-8, 7] and fp16 scales [rows, cols/128], with
+ * rows/cols as listed for FUTR_PROJ_*.  Device outputs.
+ */
+futr_status futr_unpack_weights(const futr_shape* shape, const void* blob, int32_t which,
+                                int8_t* codes, uint16_t* scales, void* stream);
+
+/* Bytes of an INT4 KV cache for n_layers x max_batch sequences of `capacity`
+ * positions (capacity is rounded up to a multiple of 16). */
+futr_status futr_kv_size(const futr_shape* shape, int32_t n_layers, int32_t max_batch,
+                         int32_t capacity, size_t* bytes);
+
+/* Zero `kv_mem`, write the RoPE cos/sin table (float64 evaluation rounded to
+ * fp32) and fill the host descriptor `kv`.  Asynchronous on `stream`. */
+futr_status futr_kv_init(const futr_shape* shape, int32_t n_layers, int32_t max_batch,
+                         int32_t capacity, void* kv_mem, size_t kv_bytes, futr_kv* kv,
+                         void* stream);
+
+/*
+ * INT4 KV-cache copy writer (abstract: "an INT4 KV-cache copy"; "A
+ * block-diagonal Hadamard transform reduces cache quantization error from
+ * outlier channels").  For sequences seq0 .. seq0+batch-1 of layer `layer`,
+ * append n_tok tokens at positions pos[b] .. pos[b]+n_tok-1 (pos: device int32
+ * [batch]).  k, v: bf16 [batch][Hkv][n_tok][d] (already position-encoded).
+ * Each (token, kv-head) vector is widened to fp32, rotated by the fp32 fast
+ * Walsh-Hadamard transform in blocks of had_block (stage s pairs i and i+2^s,
+ * ascending s, then one multiply by fp32(1/sqrt(had_block))) and quantized to
+ * INT4 with one fp16 scale, by the same rule as the weights.  Keys are stored
+ * in mma B-fragment order per 8 positions, values per 16 positions.
+ * Positions outside [0, capacity) set FUTR_ERR_OUT_OF_RANGE in the cache's
+ * error word (see futr_check) and are skipped.
+ */
+futr_status futr_kv_append(const futr_kv* kv, int32_t layer, int32_t seq0, int32_t batch,
+                           const int32_t* pos, int32_t n_tok, const uint16_t* k,
+                           const uint16_t* v, void* stream);
+
+/* Canonical view of cached entries 0..n_pos-1 of one sequence: codes int8
+ * [Hkv][n_pos][d], fp16 scales [Hkv][n_pos], for keys and values.  Device
+ * outputs. */
+futr_status futr_kv_read(const futr_kv* kv, int32_t layer, int32_t seq, int32_t n_pos,
+                         int8_t* k_codes, uint16_t* k_scales, int8_t* v_codes,
+                         uint16_t* v_scales, void* stream);
+
+/* Bytes of the workspace for decode calls with batch <= max_batch over caches
+ * of `capacity` positions. */
+futr_status futr_workspace_size(const futr_shape* shape, int32_t max_batch, int32_t capacity,
+                                size_t* bytes);
+
+/* Zero the workspace (its counters must start at 0) and fill `ws`.  The
+ * current CUDA device must be the one the workspace lives on. */
+futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int32_t capacity,
+                                void* ws_mem, size_t ws_bytes, futr_ws* ws, void* stream);
+
+/*
+ * One decode step of one block for `batch` sequences (abstract: "Decode uses
+ * INT4 projection weights and an INT4 KV-cache copy"):
+ *   r1 = 1/sqrt(mean(x^2)+eps);  [q;k;v] = r1 * (W'qkv x);  RoPE(q, k) at pos[b];
+ *   q' = fp16(H q / sqrt(n)); the new k, v are rotated, quantized and stored in
+ *   slot pos[b] of the cache (direct KV-cache placement);
+ *   o = bf16(H^T softmax(q' K'^T / sqrt(d)) V' / sqrt(n)) over slots 0..pos[b]
+ *   (grouped-query: q-head h reads kv-head h / (Hq/Hkv));
+ *   h = bf16(x + Wo o);  r2 = 1/sqrt(mean(h^2)+eps);
+ *   a = bf16(silu(r2 W'gate h) * (r2 W'up h));  y = bf16(h + Wdown a).
+ * x, y: bf16 [batch][H] (may not alias).  pos: device int32 [batch], the number
+ * of tokens already cached per sequence (sequence b uses cache slot b).
+ * blob: packed weights of this layer.  Five kernels, launched back to back with
+ * programmatic dependent launch; capturable in a CUDA graph.
+ */
+futr_status futr_decode_block(const uint16_t* x, const void* blob, const futr_kv* kv,
+                              int32_t layer, int32_t batch, const int32_t* pos, uint16_t* y,
+                              const futr_ws* ws, void* stream);
+
+/* As futr_decode_block, with a CUDA event recorded before each of the five
+ * kernels and after the last (without programmatic overlap).  Synchronizes
+ * `stream` and writes the five kernel times in milliseconds to
+ * stage_ms_host[5] (QKV, attention, O, gate/up, down). */
+futr_status futr_decode_block_timed(const uint16_t* x, const void* blob, const futr_kv* kv,
+                                    int32_t layer, int32_t batch, const int32_t* pos,
+                                    uint16_t* y, const futr_ws* ws, void* stream,
+                                    float* stage_ms_host);
+
+/* As futr_decode_block with HOST input and output: copies x_host (bf16
+ * [batch][H]) and pos_host (int32 [batch]) into the workspace, runs the block,
+ * copies y back to y_host and synchronizes `stream`.  Pinned host buffers give
+ * asynchronous copies. */
+futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, const futr_kv* kv,
+                                   int32_t layer, int32_t batch, const int32_t* pos_host,
+                                   uint16_t* y_host, const futr_ws* ws, void* stream);
+
+/* Synchronize `stream`, then return (and clear) the first nonzero device error
+ * word of the workspace `ws` and of the cache `kv` (either may be NULL), or
+ * FUTR_ERR_CUDA if a CUDA error is pending. */
+futr_status futr_check(const futr_ws* ws, const futr_kv* kv, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUTR_H_ */

@@ -1,0 +1,487 @@
+// C ABI of libfutr.so (declared in include/futr.h): argument checking, memory
+// layouts of the KV cache and the workspace, launch planning, and the five
+// launches of one decode step.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include "futr_internal.cuh"
+#include "proj.cuh"
+
+using namespace futr;
+
+namespace {
+
+constexpr int kVersion = 10000;
+
+inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+bool shape_ok(const futr_shape* s) {
+  if (!s) return false;
+  const int d = s->head_dim;
+  if (s->hidden <= 0 || s->hidden % 128) return false;
+  if (d != 64 && d != 128) return false;
+  if (s->n_q_heads <= 0 || s->n_kv_heads <= 0 || s->n_q_heads % s->n_kv_heads) return false;
+  if (s->n_q_heads / s->n_kv_heads > 16) return false;
+  if ((s->n_q_heads * d) % 128 || ((s->n_q_heads + 2 * s->n_kv_heads) * d) % 128) return false;
+  if (s->inter <= 0 || s->inter % 128) return false;
+  if (s->group != 128) return false;
+  const int nh = s->had_block;
+  if (nh < 2 || nh > d || (nh & (nh - 1))) return false;
+  if (!(s->rms_eps > 0.f) || !(s->rope_theta > 0.f)) return false;
+  return true;
+}
+
+bool same_shape(const futr_shape& a, const futr_shape& b) { return std::memcmp(&a, &b, sizeof(a)) == 0; }
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int env_int(const char* name) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : 0;
+}
+
+int round16(int c) { return (c + 15) & ~15; }
+
+struct Plans {
+  ProjPlan proj[4];  // QKV, O, GU, DOWN
+  AttnPlan attn;
+};
+
+Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
+  const BlobSections sec = blob_sections(s);
+  const int force = env_int("FUTR_SPLITK");
+  Plans p;
+  for (int i = 0; i < 4; ++i) p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force);
+  p.attn = plan_attention(s, batch, cap, n_sm, env_int("FUTR_CHUNK"));
+  return p;
+}
+
+struct WsLayout {
+  uint64_t err, qrot, o, h, a, xin, yout, pos, part, part_bytes, apart, apart_bytes, cnt, cnt_words, total;
+};
+
+WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
+  WsLayout L{};
+  const uint64_t B = (uint64_t)max_batch;
+  const uint64_t qd = (uint64_t)s.n_q_heads * s.head_dim;
+  uint64_t off = 0;
+  L.err = off; off = align256(off + 16);
+  L.qrot = off; off = align256(off + B * qd * 2);
+  L.o = off; off = align256(off + B * qd * 2);
+  L.h = off; off = align256(off + B * s.hidden * 2);
+  L.a = off; off = align256(off + B * s.inter * 2);
+  L.xin = off; off = align256(off + B * s.hidden * 2);
+  L.yout = off; off = align256(off + B * s.hidden * 2);
+  L.pos = off; off = align256(off + B * 4);
+  size_t part = 0, apart = 0;
+  for (int b = 1; b <= max_batch; ++b) {
+    const Plans p = make_plans(s, b, cap, n_sm);
+    for (int i = 0; i < 4; ++i)
+      if (p.proj[i].S > 1 && p.proj[i].part_floats > part) part = p.proj[i].part_floats;
+    if (p.attn.part_floats > apart) apart = p.attn.part_floats;
+  }
+  L.part = off; L.part_bytes = part * 4; off = align256(off + L.part_bytes);
+  L.apart = off; L.apart_bytes = apart * 4; off = align256(off + L.apart_bytes);
+  const BlobSections sec = blob_sections(s);
+  uint64_t cnt = (uint64_t)max_batch * s.n_kv_heads;
+  for (int i = 0; i < 4; ++i) cnt += sec.rows[i] / kRowsPerBlock;
+  L.cnt = off; L.cnt_words = cnt; off = align256(off + cnt * 4);
+  L.total = off;
+  return L;
+}
+
+struct KvLayout {
+  uint64_t stream_bytes, rope, err, total;
+};
+
+KvLayout kv_layout(const futr_shape& s, int n_layers, int max_batch, int cap16) {
+  KvLayout L{};
+  L.stream_bytes = kv_stream_bytes(cap16, s.head_dim);
+  uint64_t off = align256((uint64_t)n_layers * max_batch * s.n_kv_heads * L.stream_bytes);
+  L.rope = off;
+  off = align256(off + (uint64_t)cap16 * (s.head_dim / 2) * 8);
+  L.err = off;
+  L.total = align256(off + 16);
+  return L;
+}
+
+bool kv_ok(const futr_kv* kv) { return kv && kv->magic == kKvMagic && kv->base; }
+bool ws_ok(const futr_ws* ws) { return ws && ws->magic == kWsMagic && ws->base; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+template <class T>
+T* at(void* base, uint64_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(base) + off);
+}
+
+futr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FUTR_OK : FUTR_ERR_CUDA; }
+
+// Shared argument checks of the decode entry points.
+futr_status check_decode(const void* blob, const futr_kv* kv, int layer, int batch, const futr_ws* ws) {
+  if (!blob || !kv_ok(kv) || !ws_ok(ws)) return FUTR_ERR_INVALID_ARG;
+  if (!same_shape(kv->shape, ws->shape)) return FUTR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= kv->n_layers) return FUTR_ERR_INVALID_ARG;
+  if (batch < 1 || batch > kMaxBatch) return FUTR_ERR_UNSUPPORTED;
+  if (batch > kv->max_batch || batch > ws->max_batch) return FUTR_ERR_INVALID_ARG;
+  if (kv->capacity > ws->capacity) return FUTR_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(blob) & 15) != 0) return FUTR_ERR_INVALID_ARG;
+  return FUTR_OK;
+}
+
+// The five kernels of one decode step.  events: NULL, or 6 events recorded
+// around the launches (then launched without programmatic overlap).
+futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, int layer, int batch,
+                      const int32_t* pos, uint16_t* y, const futr_ws* ws, cudaStream_t st,
+                      cudaEvent_t* events) {
+  const futr_shape& s = ws->shape;
+  const Plans P = make_plans(s, batch, kv->capacity, ws->n_sm);
+  for (int i = 0; i < 4; ++i)
+    if (P.proj[i].S > 1 && P.proj[i].part_floats * 4 > ws->part_bytes) return FUTR_ERR_INVALID_ARG;
+  if (P.attn.part_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
+  const BlobSections sec = blob_sections(s);
+  const uint8_t* wb = reinterpret_cast<const uint8_t*>(blob);
+  void* base = ws->base;
+  int* err = at<int>(base, ws->off_err);
+  unsigned* cnt = at<unsigned>(base, ws->off_cnt);
+  float* part = at<float>(base, ws->off_part);
+  __half* qrot = at<__half>(base, ws->off_qrot);
+  __nv_bfloat16* o = at<__nv_bfloat16>(base, ws->off_o);
+  __nv_bfloat16* h = at<__nv_bfloat16>(base, ws->off_h);
+  __nv_bfloat16* a = at<__nv_bfloat16>(base, ws->off_a);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(y);
+  const bool pdl = events == nullptr;
+  const KvView kvl = kv_layer_view(*kv, layer);
+  const float had_c = (float)(1.0 / std::sqrt((double)s.had_block));
+
+  ProjArgs base_args{};
+  base_args.batch = batch;
+  base_args.part = part;
+  base_args.err = err;
+  base_args.eps = s.rms_eps;
+  unsigned* cnt_next = cnt;
+
+  cudaError_t e;
+  // S2: QKV + RMSNorm factor + RoPE + rotation + INT4 KV placement
+  {
+    ProjArgs A = base_args;
+    A.w = wb + sec.off[0];
+    A.xin = xb;
+    A.K = sec.cols[0];
+    A.cnt = cnt_next;
+    A.blob_magic = reinterpret_cast<const uint64_t*>(blob);
+    A.qrot = qrot;
+    A.kv = kvl;
+    A.pos = pos;
+    A.rope = at<const float2>(kv->base, kv->rope_offset);
+    A.Hq = s.n_q_heads;
+    A.Hkv = s.n_kv_heads;
+    A.d = s.head_dim;
+    A.nh = s.had_block;
+    A.had_c = had_c;
+    if (events) cudaEventRecord(events[0], st);
+    e = launch_projection(kEpiQkv, P.proj[0], A, st, pdl);
+    if (e != cudaSuccess) return FUTR_ERR_CUDA;
+    cnt_next += P.proj[0].n_rb;
+  }
+  // S3: attention
+  {
+    AttnArgs A{};
+    A.qrot = qrot;
+    A.kv = kvl;
+    A.pos = pos;
+    A.batch = batch;
+    A.Hq = s.n_q_heads;
+    A.Hkv = s.n_kv_heads;
+    A.G = s.n_q_heads / s.n_kv_heads;
+    A.nh = s.had_block;
+    A.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
+    A.had_c = had_c;
+    A.apart = at<float>(base, ws->off_apart);
+    A.cnt = cnt_next;
+    A.out = o;
+    A.err = err;
+    if (events) cudaEventRecord(events[1], st);
+    e = launch_attention(P.attn, A, s.head_dim, st, pdl);
+    if (e != cudaSuccess) return FUTR_ERR_CUDA;
+    cnt_next += (size_t)ws->max_batch * s.n_kv_heads;
+  }
+  // S4: O projection + residual
+  {
+    ProjArgs A = base_args;
+    A.w = wb + sec.off[1];
+    A.xin = o;
+    A.K = sec.cols[1];
+    A.cnt = cnt_next;
+    A.resid = xb;
+    A.out = h;
+    A.out_ld = s.hidden;
+    if (events) cudaEventRecord(events[2], st);
+    e = launch_projection(kEpiResid, P.proj[1], A, st, pdl);
+    if (e != cudaSuccess) return FUTR_ERR_CUDA;
+    cnt_next += P.proj[1].n_rb;
+  }
+  // S5: gate/up + RMSNorm factor + SwiGLU
+  {
+    ProjArgs A = base_args;
+    A.w = wb + sec.off[2];
+    A.xin = h;
+    A.K = sec.cols[2];
+    A.cnt = cnt_next;
+    A.out = a;
+    A.out_ld = s.inter;
+    if (events) cudaEventRecord(events[3], st);
+    e = launch_projection(kEpiSwiglu, P.proj[2], A, st, pdl);
+    if (e != cudaSuccess) return FUTR_ERR_CUDA;
+    cnt_next += P.proj[2].n_rb;
+  }
+  // S6: down projection + residual
+  {
+    ProjArgs A = base_args;
+    A.w = wb + sec.off[3];
+    A.xin = a;
+    A.K = sec.cols[3];
+    A.cnt = cnt_next;
+    A.resid = h;
+    A.out = yb;
+    A.out_ld = s.hidden;
+    if (events) cudaEventRecord(events[4], st);
+    e = launch_projection(kEpiResid, P.proj[3], A, st, pdl);
+    if (e != cudaSuccess) return FUTR_ERR_CUDA;
+    if (events) cudaEventRecord(events[5], st);
+  }
+  return FUTR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* futr_status_string(futr_status s) {
+  switch (s) {
+    case FUTR_OK: return "ok";
+    case FUTR_ERR_INVALID_ARG: return "invalid argument";
+    case FUTR_ERR_UNSUPPORTED: return "unsupported shape or batch";
+    case FUTR_ERR_CUDA: return "CUDA error";
+    case FUTR_ERR_OUT_OF_RANGE: return "position outside the KV cache";
+    case FUTR_ERR_TIMEOUT: return "device wait timed out";
+    case FUTR_ERR_BAD_BLOB: return "weight blob header mismatch";
+    default: return "unknown status";
+  }
+}
+
+int32_t futr_version(void) { return kVersion; }
+
+futr_status futr_weights_size(const futr_shape* shape, size_t* bytes) {
+  if (!bytes) return FUTR_ERR_INVALID_ARG;
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  *bytes = (size_t)blob_sections(*shape).total;
+  return FUTR_OK;
+}
+
+futr_status futr_pack_weights(const futr_shape* shape, const float* wq, const float* wk, const float* wv,
+                              const float* wo, const float* wgate, const float* wup, const float* wdown,
+                              const float* g_attn, const float* g_mlp, void* blob, size_t blob_bytes,
+                              void* stream) {
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  if (!wq || !wk || !wv || !wo || !wgate || !wup || !wdown || !g_attn || !g_mlp || !blob)
+    return FUTR_ERR_INVALID_ARG;
+  if (blob_bytes < blob_sections(*shape).total || (reinterpret_cast<uintptr_t>(blob) & 255))
+    return FUTR_ERR_INVALID_ARG;
+  return cuda_status(launch_pack(*shape, wq, wk, wv, wo, wgate, wup, wdown, g_attn, g_mlp,
+                                 reinterpret_cast<uint8_t*>(blob), as_stream(stream)));
+}
+
+futr_status futr_unpack_weights(const futr_shape* shape, const void* blob, int32_t which, int8_t* codes,
+                                uint16_t* scales, void* stream) {
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  if (!blob || !codes || !scales || which < FUTR_PROJ_QKV || which > FUTR_PROJ_DOWN) return FUTR_ERR_INVALID_ARG;
+  return cuda_status(launch_unpack(*shape, reinterpret_cast<const uint8_t*>(blob), which, codes, scales,
+                                   as_stream(stream)));
+}
+
+futr_status futr_kv_size(const futr_shape* shape, int32_t n_layers, int32_t max_batch, int32_t capacity,
+                         size_t* bytes) {
+  if (!bytes) return FUTR_ERR_INVALID_ARG;
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  if (n_layers < 1 || max_batch < 1 || capacity < 1) return FUTR_ERR_INVALID_ARG;
+  if (capacity > kMaxCapacity) return FUTR_ERR_UNSUPPORTED;
+  *bytes = (size_t)kv_layout(*shape, n_layers, max_batch, round16(capacity)).total;
+  return FUTR_OK;
+}
+
+futr_status futr_kv_init(const futr_shape* shape, int32_t n_layers, int32_t max_batch, int32_t capacity,
+                         void* kv_mem, size_t kv_bytes, futr_kv* kv, void* stream) {
+  if (!kv || !kv_mem) return FUTR_ERR_INVALID_ARG;
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  if (n_layers < 1 || max_batch < 1 || capacity < 1) return FUTR_ERR_INVALID_ARG;
+  if (capacity > kMaxCapacity) return FUTR_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(kv_mem) & 255) return FUTR_ERR_INVALID_ARG;
+  const int cap = round16(capacity);
+  const KvLayout L = kv_layout(*shape, n_layers, max_batch, cap);
+  if (kv_bytes < L.total) return FUTR_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  cudaError_t e = cudaMemsetAsync(kv_mem, 0, L.total, st);
+  if (e != cudaSuccess) return FUTR_ERR_CUDA;
+  e = launch_rope_table(at<float2>(kv_mem, L.rope), cap, shape->head_dim, shape->rope_theta, st);
+  if (e != cudaSuccess) return FUTR_ERR_CUDA;
+  futr_kv d{};
+  d.shape = *shape;
+  d.n_layers = n_layers;
+  d.max_batch = max_batch;
+  d.capacity = cap;
+  d.base = kv_mem;
+  d.bytes = L.total;
+  d.stream_bytes = L.stream_bytes;
+  d.rope_offset = L.rope;
+  d.err_offset = L.err;
+  d.magic = kKvMagic;
+  *kv = d;
+  return FUTR_OK;
+}
+
+futr_status futr_kv_append(const futr_kv* kv, int32_t layer, int32_t seq0, int32_t batch, const int32_t* pos,
+                           int32_t n_tok, const uint16_t* k, const uint16_t* v, void* stream) {
+  if (!kv_ok(kv) || !pos || !k || !v) return FUTR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= kv->n_layers || batch < 1 || seq0 < 0 || seq0 + batch > kv->max_batch)
+    return FUTR_ERR_INVALID_ARG;
+  if (n_tok < 1 || n_tok > kv->capacity) return FUTR_ERR_INVALID_ARG;
+  return cuda_status(launch_kv_append(*kv, layer, seq0, batch, pos, n_tok, k, v,
+                                      at<int>(kv->base, kv->err_offset), as_stream(stream)));
+}
+
+futr_status futr_kv_read(const futr_kv* kv, int32_t layer, int32_t seq, int32_t n_pos, int8_t* k_codes,
+                         uint16_t* k_scales, int8_t* v_codes, uint16_t* v_scales, void* stream) {
+  if (!kv_ok(kv) || !k_codes || !k_scales || !v_codes || !v_scales) return FUTR_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= kv->n_layers || seq < 0 || seq >= kv->max_batch) return FUTR_ERR_INVALID_ARG;
+  if (n_pos < 1 || n_pos > kv->capacity) return FUTR_ERR_INVALID_ARG;
+  return cuda_status(launch_kv_read(*kv, layer, seq, n_pos, k_codes, k_scales, v_codes, v_scales,
+                                    as_stream(stream)));
+}
+
+futr_status futr_workspace_size(const futr_shape* shape, int32_t max_batch, int32_t capacity, size_t* bytes) {
+  if (!bytes) return FUTR_ERR_INVALID_ARG;
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  if (max_batch < 1 || max_batch > kMaxBatch || capacity < 1) return FUTR_ERR_INVALID_ARG;
+  if (capacity > kMaxCapacity) return FUTR_ERR_UNSUPPORTED;
+  const int n_sm = current_sm_count();
+  if (n_sm <= 0) return FUTR_ERR_CUDA;
+  *bytes = (size_t)ws_layout(*shape, max_batch, round16(capacity), n_sm).total;
+  return FUTR_OK;
+}
+
+futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int32_t capacity, void* ws_mem,
+                                size_t ws_bytes, futr_ws* ws, void* stream) {
+  if (!ws || !ws_mem) return FUTR_ERR_INVALID_ARG;
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  if (max_batch < 1 || max_batch > kMaxBatch || capacity < 1) return FUTR_ERR_INVALID_ARG;
+  if (capacity > kMaxCapacity) return FUTR_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(ws_mem) & 255) return FUTR_ERR_INVALID_ARG;
+  const int n_sm = current_sm_count();
+  if (n_sm <= 0) return FUTR_ERR_CUDA;
+  const int cap = round16(capacity);
+  const WsLayout L = ws_layout(*shape, max_batch, cap, n_sm);
+  if (ws_bytes < L.total) return FUTR_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(ws_mem, 0, L.total, as_stream(stream)) != cudaSuccess) return FUTR_ERR_CUDA;
+  futr_ws d{};
+  d.shape = *shape;
+  d.max_batch = max_batch;
+  d.capacity = cap;
+  d.n_sm = n_sm;
+  d.base = ws_mem;
+  d.bytes = L.total;
+  d.off_err = L.err;
+  d.off_qrot = L.qrot;
+  d.off_o = L.o;
+  d.off_h = L.h;
+  d.off_a = L.a;
+  d.off_xin = L.xin;
+  d.off_yout = L.yout;
+  d.off_pos = L.pos;
+  d.off_part = L.part;
+  d.part_bytes = L.part_bytes;
+  d.off_apart = L.apart;
+  d.apart_bytes = L.apart_bytes;
+  d.off_cnt = L.cnt;
+  d.cnt_words = L.cnt_words;
+  d.magic = kWsMagic;
+  *ws = d;
+  return FUTR_OK;
+}
+
+futr_status futr_decode_block(const uint16_t* x, const void* blob, const futr_kv* kv, int32_t layer,
+                              int32_t batch, const int32_t* pos, uint16_t* y, const futr_ws* ws, void* stream) {
+  if (!x || !pos || !y || x == y) return FUTR_ERR_INVALID_ARG;
+  const futr_status st = check_decode(blob, kv, layer, batch, ws);
+  if (st != FUTR_OK) return st;
+  return run_block(x, blob, kv, layer, batch, pos, y, ws, as_stream(stream), nullptr);
+}
+
+futr_status futr_decode_block_timed(const uint16_t* x, const void* blob, const futr_kv* kv, int32_t layer,
+                                    int32_t batch, const int32_t* pos, uint16_t* y, const futr_ws* ws,
+                                    void* stream, float* stage_ms_host) {
+  if (!x || !pos || !y || x == y || !stage_ms_host) return FUTR_ERR_INVALID_ARG;
+  futr_status st = check_decode(blob, kv, layer, batch, ws);
+  if (st != FUTR_OK) return st;
+  cudaEvent_t ev[6];
+  for (int i = 0; i < 6; ++i)
+    if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      return FUTR_ERR_CUDA;
+    }
+  cudaStream_t s = as_stream(stream);
+  st = run_block(x, blob, kv, layer, batch, pos, y, ws, s, ev);
+  if (st == FUTR_OK && cudaStreamSynchronize(s) != cudaSuccess) st = FUTR_ERR_CUDA;
+  for (int i = 0; i < 5 && st == FUTR_OK; ++i)
+    if (cudaEventElapsedTime(&stage_ms_host[i], ev[i], ev[i + 1]) != cudaSuccess) st = FUTR_ERR_CUDA;
+  for (int i = 0; i < 6; ++i) cudaEventDestroy(ev[i]);
+  return st;
+}
+
+futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, const futr_kv* kv, int32_t layer,
+                                   int32_t batch, const int32_t* pos_host, uint16_t* y_host, const futr_ws* ws,
+                                   void* stream) {
+  if (!x_host || !pos_host || !y_host) return FUTR_ERR_INVALID_ARG;
+  futr_status st = check_decode(blob, kv, layer, batch, ws);
+  if (st != FUTR_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  const size_t xb = (size_t)batch * ws->shape.hidden * 2;
+  uint16_t* xd = at<uint16_t>(ws->base, ws->off_xin);
+  uint16_t* yd = at<uint16_t>(ws->base, ws->off_yout);
+  int32_t* pd = at<int32_t>(ws->base, ws->off_pos);
+  if (cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return FUTR_ERR_CUDA;
+  if (cudaMemcpyAsync(pd, pos_host, (size_t)batch * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FUTR_ERR_CUDA;
+  st = run_block(xd, blob, kv, layer, batch, pd, yd, ws, s, nullptr);
+  if (st != FUTR_OK) return st;
+  if (cudaMemcpyAsync(y_host, yd, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return FUTR_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(s));
+}
+
+futr_status futr_check(const futr_ws* ws, const futr_kv* kv, void* stream) {
+  cudaStream_t s = as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FUTR_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FUTR_ERR_CUDA;
+  futr_status result = FUTR_OK;
+  int* words[2] = {ws_ok(ws) ? at<int>(ws->base, ws->off_err) : nullptr,
+                   kv_ok(kv) ? at<int>(kv->base, kv->err_offset) : nullptr};
+  for (int i = 0; i < 2; ++i) {
+    if (!words[i]) continue;
+    int v = 0;
+    if (cudaMemcpy(&v, words[i], sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FUTR_ERR_CUDA;
+    if (v != 0) {
+      if (result == FUTR_OK) result = v;
+      if (cudaMemset(words[i], 0, sizeof(int)) != cudaSuccess) return FUTR_ERR_CUDA;
+    }
+  }
+  return result;
+}
+
+}  // extern "C"

@@ -1,0 +1,353 @@
+// Internal definitions shared by the libfutr kernels: packed layouts, PTX
+// wrappers (mbarrier, bulk async copy, programmatic dependent launch,
+// mma.sync, ldmatrix) and the fp32 rotation + INT4 quantizer used by both KV
+// writers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "futr.h"
+
+namespace futr {
+
+// ----------------------------------------------------------------- layouts --
+// Packed weights: a projection with N output rows and K inputs is cut into
+// units of 128 rows x 128 inputs (one scale group).  Unit (rb, g) sits at
+// byte ((rb * K/128) + g) * kUnitBytes of its section:
+//   8 row tiles of 16 rows, each [half 0..1][lane 0..31][16 bytes]:
+//     lane = 4*gr + t holds, for the k-steps ks = 4*half + j (j = word 0..3),
+//     one 32-bit word with the 8 nibbles (code + 8) of rows gr, gr+8 and
+//     columns 16ks + {2t, 2t+1, 2t+8, 2t+9}: nibble i (bits 4i..4i+3) is the
+//     low half of register a_i, nibble i+4 its high half, where a0 = (gr, 2t),
+//     a1 = (gr+8, 2t), a2 = (gr, 2t+8), a3 = (gr+8, 2t+8) -- the m16n8k16 A
+//     fragment of that lane.
+//   then 128 fp16 scales, one per row of the unit.
+constexpr int kRowsPerBlock = 128;
+constexpr int kGroup = 128;
+constexpr int kUnitCodeBytes = kRowsPerBlock * kGroup / 2;   // 8192
+constexpr int kUnitBytes = kUnitCodeBytes + kRowsPerBlock * 2; // 8448
+constexpr int kHeaderBytes = 256;
+constexpr uint64_t kBlobMagic = 0x3141345754554631ull;         // "1FUTW4A1"
+constexpr uint64_t kKvMagic = 0x31564b3452545546ull;
+constexpr uint64_t kWsMagic = 0x3153573452545546ull;
+constexpr int kMaxBatch = 32;
+constexpr int kMaxCapacity = 65536;  // positions per sequence (chunk-merge scratch bound)
+
+// KV stream of one (layer, seq, kv-head), capacity C (multiple of 16):
+//   K codes: C/8 tiles of 8 positions x d/2 bytes; in a tile, lane 4*p + t
+//     (p = position in tile) owns d/8 bytes = d/32 words; word j holds the
+//     nibbles of dims 32j + {2t, 2t+8, 16+2t, 16+2t+8} in slots 0..3 and
+//     dims 32j + {2t+1, 2t+9, 16+2t+1, 16+2t+9} in slots 4..7: slots (i, i+4)
+//     form the fp16x2 register of the B fragment (k = dims, n = positions).
+//   V codes: C/16 tiles of 16 positions x d/2 bytes; lane 4*gr + t owns d/4
+//     bytes = d/16 words; word j holds dims 16j + gr (slots 0,1,4,5) and
+//     16j + 8 + gr (slots 2,3,6,7) at tile positions 2t (slot 0/2), 2t+8
+//     (1/3), 2t+1 (4/6), 2t+9 (5/7): the B fragment with k = positions,
+//     n = dims.
+//   K scales fp16 [C], V scales fp16 [C].
+__host__ __device__ inline uint64_t kv_stream_bytes(int cap, int d) {
+  return (uint64_t)cap * (uint64_t)(d + 4);
+}
+
+struct BlobSections {
+  uint64_t off[4];   // QKV, O, GU, DOWN
+  int rows[4];
+  int cols[4];
+  uint64_t total;
+};
+
+__host__ inline BlobSections blob_sections(const futr_shape& s) {
+  BlobSections b;
+  const int qkv = (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
+  b.rows[0] = qkv;          b.cols[0] = s.hidden;
+  b.rows[1] = s.hidden;     b.cols[1] = s.n_q_heads * s.head_dim;
+  b.rows[2] = 2 * s.inter;  b.cols[2] = s.hidden;
+  b.rows[3] = s.hidden;     b.cols[3] = s.inter;
+  uint64_t off = kHeaderBytes;
+  for (int i = 0; i < 4; ++i) {
+    b.off[i] = off;
+    off += (uint64_t)(b.rows[i] / kRowsPerBlock) * (uint64_t)(b.cols[i] / kGroup) * kUnitBytes;
+    off = (off + 255) & ~uint64_t(255);
+  }
+  b.total = off;
+  return b;
+}
+
+struct BlobHeader {
+  uint64_t magic;
+  int32_t version;
+  int32_t _pad;
+  futr_shape shape;
+};
+
+// ------------------------------------------------------------ PTX helpers --
+constexpr unsigned long long kWaitNs = 1000000000ull;  // bounded waits: 1 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with parity `parity` until the %globaltimer
+// `deadline` (ns); returns false when it passed (the caller records
+// FUTR_ERR_TIMEOUT and stops waiting).
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, unsigned long long deadline) {
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 15u && global_ns() > deadline) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Programmatic dependent launch: no-ops when the kernel was launched without it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(smem_row)));
+}
+
+// Nibble pair (bits 4i and 16+4i of w, offset-8 codes) -> exact bf16x2 codes:
+// 0x4300 | u is the bf16 value 128 + u; subtracting 136 leaves u - 8.
+__device__ __forceinline__ uint32_t nib_bf16x2(uint32_t w, int i) {
+  uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
+  v = __hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Same for fp16: 0x6400 | u is 1024 + u; subtracting 1032 leaves u - 8.
+__device__ __forceinline__ uint32_t nib_f16x2(uint32_t w, int i) {
+  uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+  __half2 v = *reinterpret_cast<__half2*>(&t);
+  v = __hsub2(v, __floats2half2_rn(1032.0f, 1032.0f));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// v0, v1 -> fp16x2 hi = (fp16(v0), fp16(v1)) and lo = fp16 of the remainders.
+__device__ __forceinline__ void split_half2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(v0, v1);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ void set_err(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ------------------------------------------------- rotation + quantizer --
+// One warp holds a d-vector (d = 32*J, element i = lane + 32*j in v[j]).
+// fp32 fast Walsh-Hadamard transform in blocks of nh (power of two <= d):
+// stage s pairs i (bit s clear) with i + 2^s -> (a + b, a - b), ascending s;
+// then one multiply by c = fp32(1/sqrt(nh)).
+template <int J>
+__device__ __forceinline__ void warp_fwht(float (&v)[J], int nh, float c) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {
+    if (h < nh) {
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const float p = __shfl_xor_sync(0xffffffffu, v[j], h);
+        v[j] = (lane & h) ? __fsub_rn(p, v[j]) : __fadd_rn(v[j], p);
+      }
+    }
+  }
+#pragma unroll
+  for (int hj = 1; hj < J; hj <<= 1) {
+    if (32 * hj < nh) {
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        if ((j & hj) == 0) {
+          const float a = v[j], b = v[j + hj];
+          v[j] = __fadd_rn(a, b);
+          v[j + hj] = __fsub_rn(a, b);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < J; ++j) v[j] = __fmul_rn(v[j], c);
+}
+
+// INT4 round-to-nearest of a warp-held vector: s = fp16(max|v| / 7) (fp32
+// division, saturating at 65504), code = clamp(rint(v / s), -8, 7), 0 if s == 0.
+template <int J>
+__device__ __forceinline__ __half warp_quant(const float (&v)[J], int (&code)[J]) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < J; ++j) m = fmaxf(m, fabsf(v[j]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const __half s = __float2half_rn(fminf(__fdiv_rn(m, 7.0f), 65504.0f));
+  const float sf = __half2float(s);
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    int c = 0;
+    if (sf > 0.f) {
+      c = __float2int_rn(__fdiv_rn(v[j], sf));
+      c = c < -8 ? -8 : (c > 7 ? 7 : c);
+    }
+    code[j] = c;
+  }
+  return s;
+}
+
+// Device view of one layer of the KV cache.
+struct KvView {
+  uint8_t* base;            // stream (layer, seq 0, kvh 0)
+  uint64_t stream_bytes;
+  int cap, d, n_kv;
+  __device__ __forceinline__ uint8_t* stream(int seq, int kvh) const {
+    return base + ((uint64_t)seq * n_kv + kvh) * stream_bytes;
+  }
+};
+
+// Write the codes (warp-held code[j] of dim lane+32j, codes in [-8,7]) and
+// scale of one token of one kv-head into slot p of a stream.  `scratch`:
+// per-warp shared buffer of d bytes.  K slots are plain stores of whole
+// words; V slots are read-modify-write of the nibbles of position p only, so
+// a caller must not write two positions of the same 16-position tile
+// concurrently from different warps.
+template <int J>
+__device__ __forceinline__ void store_k_token(uint8_t* strm, int cap, int p, const int (&code)[J],
+                                              __half s, int8_t* scratch) {
+  constexpr int d = 32 * J;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < J; ++j) scratch[lane + 32 * j] = (int8_t)code[j];
+  __syncwarp();
+  // d/8 words per position: lane index within position t = w / (d/32), word j = w % (d/32)
+  if (lane < d / 8) {
+    const int t = lane / (d / 32), j = lane % (d / 32);
+    const int base = 32 * j + 2 * t;
+    const int dims[8] = {base, base + 8, base + 16, base + 24, base + 1, base + 9, base + 17, base + 25};
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= (uint32_t)((scratch[dims[i]] + 8) & 0xF) << (4 * i);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(strm + (uint64_t)(p >> 3) * (4 * d) + (p & 7) * (d / 2));
+    dst[lane] = w;
+  }
+  if (lane == 0) {
+    __half* ks = reinterpret_cast<__half*>(strm + (uint64_t)cap * d);
+    ks[p] = s;
+  }
+  __syncwarp();
+}
+
+template <int J>
+__device__ __forceinline__ void store_v_token(uint8_t* strm, int cap, int p, const int (&code)[J],
+                                              __half s, int8_t* scratch) {
+  constexpr int d = 32 * J;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < J; ++j) scratch[lane + 32 * j] = (int8_t)code[j];
+  __syncwarp();
+  const int p16 = p & 15;
+  const int t = (p16 & 7) >> 1, hi = p16 >> 3, odd = p16 & 1;
+  const int sh = 16 * odd + 4 * hi;
+  uint32_t* tile = reinterpret_cast<uint32_t*>(strm + (uint64_t)cap * (d / 2) + (uint64_t)(p >> 4) * (8 * d));
+  // 8 lanes (gr = 0..7) x d/16 words
+  for (int w = lane; w < 8 * (d / 16); w += 32) {
+    const int gr = w / (d / 16), j = w % (d / 16);
+    const uint32_t n0 = (uint32_t)((scratch[16 * j + gr] + 8) & 0xF);
+    const uint32_t n1 = (uint32_t)((scratch[16 * j + 8 + gr] + 8) & 0xF);
+    uint32_t* dst = tile + (4 * gr + t) * (d / 16) + j;
+    const uint32_t mask = (0xFu << sh) | (0xFu << (sh + 8));
+    *dst = (*dst & ~mask) | (n0 << sh) | (n1 << (sh + 8));
+  }
+  if (lane == 0) {
+    __half* vs = reinterpret_cast<__half*>(strm + (uint64_t)cap * d + 2ull * cap);
+    vs[p] = s;
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------- host launchers --
+cudaError_t launch_pack(const futr_shape& s, const float* wq, const float* wk, const float* wv,
+                        const float* wo, const float* wg, const float* wu, const float* wd,
+                        const float* ga, const float* gm, uint8_t* blob, cudaStream_t st);
+cudaError_t launch_unpack(const futr_shape& s, const uint8_t* blob, int which, int8_t* codes,
+                          uint16_t* scales, cudaStream_t st);
+cudaError_t launch_rope_table(float2* table, int cap, int d, float theta, cudaStream_t st);
+cudaError_t launch_kv_append(const futr_kv& kv, int layer, int seq0, int batch, const int* pos,
+                             int n_tok, const uint16_t* k, const uint16_t* v, int* err,
+                             cudaStream_t st);
+cudaError_t launch_kv_read(const futr_kv& kv, int layer, int seq, int n_pos, int8_t* kc, uint16_t* ks,
+                           int8_t* vc, uint16_t* vs, cudaStream_t st);
+KvView kv_layer_view(const futr_kv& kv, int layer);
+
+}  // namespace futr

@@ -1,0 +1,73 @@
+// Arguments and launch plans of the W4A16 projection and attention kernels.
+#pragma once
+
+#include "futr_internal.cuh"
+
+namespace futr {
+
+constexpr int kStages = 8;          // bulk-copy ring depth (units of 8448 B)
+constexpr int kRedLd = 132;         // fp32 row of the epilogue tile (bank-conflict padding)
+constexpr int kXsMax = 64 * 1024;   // activation slice budget in shared memory
+constexpr int kProjMaxSmem = 200 * 1024;
+
+constexpr int kEpiResid = 0;
+constexpr int kEpiSwiglu = 1;
+constexpr int kEpiQkv = 2;
+
+struct ProjArgs {
+  const uint8_t* w;              // section base of the packed blob
+  const __nv_bfloat16* xin;      // activations [batch][K]
+  int K, n_groups, S, batch;
+  int off_xs, off_misc, rec_floats;
+  float* part;                   // split-K partial records [n_rb][S][rec_floats]
+  unsigned* cnt;                 // arrival counters [n_rb]
+  int* err;
+  float eps;
+  // RESID / SWIGLU output
+  const __nv_bfloat16* resid;    // RESID: [batch][out_ld]
+  __nv_bfloat16* out;
+  int out_ld;
+  // QKV
+  const uint64_t* blob_magic;
+  __half* qrot;                  // [batch][Hq][d]
+  KvView kv;
+  const int* pos;
+  const float2* rope;            // [cap][d/2]
+  int Hq, Hkv, d, nh;
+  float had_c;
+};
+
+struct ProjPlan {
+  int n_rb, n_groups, nt, S;
+  int off_xs, off_misc, rec_floats;
+  size_t smem;
+  size_t part_floats;
+};
+
+ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_split);
+cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream_t st, bool pdl);
+
+struct AttnArgs {
+  const __half* qrot;            // [batch][Hq][d]
+  KvView kv;
+  const int* pos;
+  int batch, Hq, Hkv, G, nh, CH, max_chunks;
+  float qk_scale_log2;           // log2(e) / sqrt(d)
+  float had_c;
+  float* apart;                  // [batch][Hkv][max_chunks][rec]
+  int rec_floats;
+  unsigned* cnt;                 // [batch][Hkv]
+  __nv_bfloat16* out;            // [batch][Hq*d]
+  int* err;
+};
+
+struct AttnPlan {
+  int CH, max_chunks, rec_floats;
+  size_t smem;
+  size_t part_floats;
+};
+
+AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int force_chunk);
+cudaError_t launch_attention(const AttnPlan& p, AttnArgs a, int d, cudaStream_t st, bool pdl);
+
+}  // namespace futr

@@ -1,0 +1,271 @@
+"""CUDA path vs the float64 oracle, through the C ABI, on seeded inputs.
+
+Quantized codes and scales are compared bit for bit; block outputs within the
+block tolerance (relative L2 <= 1e-3, max abs <= 2e-2 rms).  The oracle is
+evaluated on the identical dequantized values: its own packing (shown equal
+to the GPU's) and, for the token appended inside the step, the GPU's cache
+entries (that append depends on the fp32 accumulation order of the QKV
+projection; its codes are checked to within one step against the oracle's).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int4_weight_kv_w4a16_gb300 import futr, inputs
+from int4_weight_kv_w4a16_gb300.inputs import LLAMA8B, LLAMA70B, TOY, WORKLOADS
+from tests._gpu_helpers import GpuBlock, assert_close, bits_to_f64, dev, errors, oracle_case
+
+pytestmark = pytest.mark.gpu
+
+# Stage-wise bound for a projection fed the GPU's own input: fp32 vs float64
+# accumulation (~1e-6) plus rare one-ulp flips at the bf16 output rounding.
+STAGE_REL = 3e-4
+ERRORS = []
+
+
+def record_errors(shape, batch, errs):
+    ERRORS.append({"hidden": shape.hidden, "batch": batch, **errs})
+    import json, os
+    os.makedirs("gpurun_out", exist_ok=True)
+    with open("gpurun_out/parity_errors.jsonl", "a") as f:
+        f.write(json.dumps(ERRORS[-1]) + "\n")
+
+
+PROJ = {"qkv": futr.FUTR_PROJ_QKV, "o": futr.FUTR_PROJ_O, "gate": futr.FUTR_PROJ_GATE,
+        "up": futr.FUTR_PROJ_UP, "down": futr.FUTR_PROJ_DOWN}
+
+
+def check_pack(gpu, packed):
+    for name, which in PROJ.items():
+        c, s = gpu.unpack(which)
+        np.testing.assert_array_equal(c, packed[name][0], err_msg=name)
+        np.testing.assert_array_equal(s.view(np.uint16), packed[name][1].view(np.uint16), err_msg=name)
+
+
+def check_new_token(ref, gpu_new, b):
+    kc, ks, vc, vs = gpu_new
+    for a, r in ((kc, ref["k_codes"]), (vc, ref["v_codes"])):
+        assert np.abs(a.astype(int) - r.astype(int)).max() <= 1
+        assert np.mean(a != r) < 0.01
+    for a, r in ((ks, ref["k_scales"]), (vs, ref["v_scales"])):
+        a64, r64 = a.astype(np.float64), r.astype(np.float64)
+        assert np.all(np.abs(a64 - r64) <= np.abs(r64) * 2.0 ** -10 + 1e-30)
+
+
+def run_case(shape, batch, lengths, seed=0, n_outlier=4, chunks=None, check_codes=True):
+    weights = inputs.block_weights(shape, seed)
+    x = inputs.activations(shape, batch, seed)
+    hist = inputs.kv_history(shape, lengths, n_outlier=n_outlier, seed=seed)
+    cap = int(max(lengths)) + 16
+    gpu = GpuBlock(shape, weights, max_batch=batch, capacity=cap)
+    gpu.append_history(0, hist, chunks=chunks)
+    pos = np.asarray(lengths, dtype=np.int32)
+    y = gpu.decode(x, pos)
+    ref, packed, cache, gcache = oracle_case(shape, weights, x, hist, pos, gpu)
+    if check_codes:
+        check_pack(gpu, packed)
+        for i in range(batch):
+            L = int(pos[i])
+            for key in ("k_codes", "v_codes"):
+                np.testing.assert_array_equal(gcache[i][key][:, :L], cache[i][key][:, :L], err_msg=key)
+            for key in ("k_scales", "v_scales"):
+                np.testing.assert_array_equal(gcache[i][key][:, :L].view(np.uint16),
+                                              cache[i][key][:, :L].view(np.uint16), err_msg=key)
+    gnew = (np.stack([g["k_codes"][:, int(pos[i])] for i, g in enumerate(gcache)]),
+            np.stack([g["k_scales"][:, int(pos[i])] for i, g in enumerate(gcache)]),
+            np.stack([g["v_codes"][:, int(pos[i])] for i, g in enumerate(gcache)]),
+            np.stack([g["v_scales"][:, int(pos[i])] for i, g in enumerate(gcache)]))
+    check_new_token(ref, gnew, batch)
+    # stage by stage, each kernel fed the GPU's own input to that stage
+    inter = gpu.intermediates(batch)
+    xf = oracle.bf16_bits_to_float(x)
+    wdq = oracle.dequant_block(packed)
+    kfull = [g["k_codes"].astype(np.float64) * g["k_scales"].astype(np.float64)[..., None] for g in gcache]
+    vfull = [g["v_codes"].astype(np.float64) * g["v_scales"].astype(np.float64)[..., None] for g in gcache]
+    yg = bits_to_f64(y)
+    diag = {"e2e_" + k: errors(inter[k] if k != "y" else yg, ref[k]) for k in ("q_rot", "o", "h", "a", "y")}
+    diag["y_per_seq_rel"] = [errors(yg[i], ref["y"][i])["rel_l2"] for i in range(batch)]
+    diag["o_per_seq_rel"] = [errors(inter["o"][i], ref["o"][i])["rel_l2"] for i in range(batch)]
+    record_errors(shape, batch, diag)
+    errs = {}
+    errs["q_rot"] = assert_close(inter["q_rot"], oracle.stage_qkv(xf, wdq["qkv"], pos, shape)["q_rot"], "q_rot",
+                                 rel=STAGE_REL, flip=True)
+    errs["o"] = assert_close(inter["o"], oracle.stage_attention(inter["q_rot"], kfull, vfull, shape), "o",
+                            rel=STAGE_REL, flip=True)
+    errs["h"] = assert_close(inter["h"], oracle.stage_o(xf, inter["o"], wdq["o"]), "h", rel=STAGE_REL, flip=True)
+    errs["a"] = assert_close(inter["a"], oracle.stage_mlp_in(inter["h"], wdq["gate"], wdq["up"], shape.rms_eps),
+                             "a", rel=STAGE_REL, flip=True)
+    errs["y_stage"] = assert_close(yg, oracle.stage_down(inter["h"], inter["a"], wdq["down"]), "y stage",
+                                   rel=STAGE_REL, flip=True)
+    # end to end from x: the block tolerance
+    errs["y"] = assert_close(yg, ref["y"], "y")
+    record_errors(shape, batch, errs)
+    return gpu, ref, y
+
+
+# ------------------------------------------------------------ quantizers --
+
+def test_pack_bit_exact_toy():
+    w = inputs.block_weights(TOY, 0)
+    gpu = GpuBlock(TOY, w, max_batch=1, capacity=32)
+    check_pack(gpu, oracle.pack_block(w))
+
+
+def test_pack_bit_exact_special_values():
+    """All-zero groups, a single outlier per group, exact .5 quotients."""
+    w = inputs.block_weights(TOY, 3)
+    w["wo"][:] = 0.0
+    w["wo"][5, 130] = 3.0
+    w["wdown"][7, :128] = np.float32(0.25) * np.array([7, 2.5, 3.5, -2.5, -3.5, 0.5, -0.5, 1.5] * 16, np.float32)
+    gpu = GpuBlock(TOY, w, max_batch=1, capacity=32)
+    check_pack(gpu, oracle.pack_block(w))
+
+
+def test_pack_bit_exact_8b():
+    w = inputs.block_weights(LLAMA8B, 0)
+    gpu = GpuBlock(LLAMA8B, w, max_batch=1, capacity=32)
+    check_pack(gpu, oracle.pack_block(w))
+
+
+@pytest.mark.parametrize("shape", [TOY, LLAMA8B], ids=["toy", "8b"])
+def test_kv_append_bit_exact_chunked(shape):
+    """Appends that start and end inside 8- and 16-position tiles."""
+    lengths = [37, 1, 16, 100]
+    hist = inputs.kv_history(shape, lengths, seed=5)
+    gpu = GpuBlock(shape, inputs.block_weights(TOY, 0) if shape is TOY else _tiny_weights(shape),
+                   max_batch=4, capacity=128)
+    gpu.append_history(0, hist, chunks=[5, 3, 8, 17, 1, 30])
+    ref = oracle.build_cache(hist, shape)
+    for i, L in enumerate(lengths):
+        g = gpu.read_cache(0, i, L)
+        for key in ("k_codes", "v_codes"):
+            np.testing.assert_array_equal(g[key], ref[i][key], err_msg=key)
+        for key in ("k_scales", "v_scales"):
+            np.testing.assert_array_equal(g[key].view(np.uint16), ref[i][key].view(np.uint16), err_msg=key)
+    assert futr.futr_check(gpu.ws, gpu.kv) == 0
+
+
+def _tiny_weights(shape):
+    """Zero weights of the right shapes (tests that only use the cache)."""
+    z = lambda o, i: np.zeros((o, i), np.float32)
+    return {"wq": z(shape.q_rows, shape.hidden), "wk": z(shape.kv_rows, shape.hidden),
+            "wv": z(shape.kv_rows, shape.hidden), "wo": z(shape.hidden, shape.q_rows),
+            "wgate": z(shape.inter, shape.hidden), "wup": z(shape.inter, shape.hidden),
+            "wdown": z(shape.hidden, shape.inter), "g_attn": np.ones(shape.hidden, np.float32),
+            "g_mlp": np.ones(shape.hidden, np.float32)}
+
+
+def test_kv_append_out_of_range_flagged():
+    gpu = GpuBlock(TOY, _tiny_weights(TOY), max_batch=1, capacity=32)
+    k = np.zeros((TOY.n_kv_heads, 8, TOY.head_dim), np.uint16)
+    gpu.append(0, 0, k, k, 30)  # 30 + 8 > 32
+    assert futr.futr_check(gpu.ws, gpu.kv) == futr.FUTR_ERR_OUT_OF_RANGE
+    assert futr.futr_check(gpu.ws, gpu.kv) == 0  # the error word was cleared
+
+
+# ----------------------------------------------------------- whole block --
+
+def test_decode_toy_workload():
+    wl = WORKLOADS["toy_b1_ctx128"]
+    run_case(wl.shape, wl.batch, inputs.context_lengths(wl), n_outlier=wl.n_outlier)
+
+
+@pytest.mark.parametrize("batch", [1, 2, 3, 7, 8, 9, 16, 31, 32])
+def test_decode_toy_batch_sweep(batch):
+    r = np.random.default_rng(batch)
+    lengths = r.integers(0, 300, size=batch)
+    lengths[0] = 0  # empty history: attention over the new token only
+    if batch > 2:
+        lengths[1:3] = [15, 16]
+    run_case(TOY, batch, list(lengths), seed=batch, chunks=[13, 64, 200] if batch % 2 else None)
+
+
+def test_decode_8b_b1_ctx1024():
+    wl = WORKLOADS["llama8b_b1_ctx1024"]
+    run_case(wl.shape, wl.batch, inputs.context_lengths(wl))
+
+
+def test_decode_8b_b32_ragged():
+    wl = WORKLOADS["llama8b_b32_ragged512-4096"]
+    run_case(wl.shape, wl.batch, inputs.context_lengths(wl), check_codes=True)
+
+
+def test_decode_deterministic_and_splitk_invariant(monkeypatch):
+    shape, batch = TOY, 5
+    lengths = [3, 70, 129, 200, 1]
+    weights = inputs.block_weights(shape, 7)
+    x = inputs.activations(shape, batch, 7)
+    hist = inputs.kv_history(shape, lengths, seed=7)
+    pos = np.array(lengths, np.int32)
+    outs = []
+    for split in (None, None, "1", "3"):
+        if split is None:
+            monkeypatch.delenv("FUTR_SPLITK", raising=False)
+        else:
+            monkeypatch.setenv("FUTR_SPLITK", split)
+        gpu = GpuBlock(shape, weights, max_batch=batch, capacity=256)
+        gpu.append_history(0, hist)
+        outs.append(bits_to_f64(gpu.decode(x, pos)))
+    np.testing.assert_array_equal(outs[0], outs[1])  # same plan: bit-identical
+    for o in outs[2:]:
+        assert_close(o, outs[0], "split-K", rel=2e-3)
+
+
+def test_decode_x_zero_weights_zero():
+    shape = TOY
+    w = _tiny_weights(shape)
+    gpu = GpuBlock(shape, w, max_batch=2, capacity=64)
+    hist = inputs.kv_history(shape, [10, 3], seed=1)
+    gpu.append_history(0, hist)
+    y = gpu.decode(np.zeros((2, shape.hidden), np.uint16), np.array([10, 3], np.int32))
+    assert np.all(bits_to_f64(y) == 0)
+
+
+def test_decode_identity_when_wo_wdown_zero():
+    shape = TOY
+    w = inputs.block_weights(shape, 2)
+    w["wo"][:] = 0
+    w["wdown"][:] = 0
+    gpu = GpuBlock(shape, w, max_batch=3, capacity=64)
+    gpu.append_history(0, inputs.kv_history(shape, [4, 0, 33], seed=2))
+    x = inputs.activations(shape, 3, 2)
+    y = gpu.decode(x, np.array([4, 0, 33], np.int32))
+    np.testing.assert_array_equal(y.cpu().numpy().view(np.uint16), x)
+
+
+def test_decode_position_out_of_range_flagged():
+    shape = TOY
+    gpu = GpuBlock(shape, inputs.block_weights(shape, 0), max_batch=2, capacity=32)
+    x = dev(inputs.activations(shape, 2, 0).view(np.int16))
+    y = torch.empty_like(x)
+    pos = dev(np.array([5, 32], np.int32))  # slot 32 is outside a 32-position cache
+    futr.futr_decode_block(x, gpu.blob, gpu.kv, 0, 2, pos, y, gpu.ws)
+    assert futr.futr_check(gpu.ws, gpu.kv) == futr.FUTR_ERR_OUT_OF_RANGE
+    assert np.all(np.isfinite(bits_to_f64(y)))
+
+
+def test_decode_bad_blob_flagged():
+    shape = TOY
+    gpu = GpuBlock(shape, inputs.block_weights(shape, 0), max_batch=1, capacity=32)
+    gpu.blob[:8] = 0  # destroy the header magic
+    x = dev(inputs.activations(shape, 1, 0).view(np.int16))
+    y = torch.empty_like(x)
+    futr.futr_decode_block(x, gpu.blob, gpu.kv, 0, 1, dev(np.array([3], np.int32)), y, gpu.ws)
+    assert futr.futr_check(gpu.ws, gpu.kv) == futr.FUTR_ERR_BAD_BLOB
+
+
+def test_decode_host_entry_matches_device_entry():
+    shape, batch = TOY, 3
+    w = inputs.block_weights(shape, 4)
+    gpu = GpuBlock(shape, w, max_batch=batch, capacity=64)
+    gpu.append_history(0, inputs.kv_history(shape, [5, 6, 7], seed=4))
+    x = inputs.activations(shape, batch, 4)
+    pos = np.array([5, 6, 7], np.int32)
+    yd = gpu.decode(x, pos).cpu().numpy().view(np.uint16)
+    # run again through the host-buffer entry (same cache slot is rewritten identically)
+    xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+    ph = torch.from_numpy(pos.copy()).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    futr.futr_decode_block_host(xh, gpu.blob, gpu.kv, 0, batch, ph, yh, gpu.ws)
+    np.testing.assert_array_equal(yh.numpy().view(np.uint16), yd)
