@@ -80,7 +80,7 @@ typedef struct futr_ws {
   void* base;
   uint64_t bytes;
   uint64_t off_err;      /* int32 error word                                   */
-  uint64_t off_qrot;     /* fp16 [b][Hq][d]   rotated query                     */
+  uint64_t off_qrot;     /* fp32 [b][Hq][d]   rotated query                     */
   uint64_t off_o;        /* bf16 [b][Hq*d]    attention output (unrotated)      */
   uint64_t off_h;        /* bf16 [b][H]       residual after attention          */
   uint64_t off_a;        /* bf16 [b][I]       SwiGLU activation                 */
@@ -193,7 +193,7 @@ futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int3
  * One decode step of one block for `batch` sequences (abstract: "Decode uses
  * INT4 projection weights and an INT4 KV-cache copy"):
  *   r1 = 1/sqrt(mean(x^2)+eps);  [q;k;v] = r1 * (W'qkv x);  RoPE(q, k) at pos[b];
- *   q' = fp16(H q / sqrt(n)); the new k, v are rotated, quantized and stored in
+ *   q' = H q / sqrt(n) (fp32); the new k, v are rotated, quantized and stored in
  *   slot pos[b] of the cache (direct KV-cache placement);
  *   o = bf16(H^T softmax(q' K'^T / sqrt(d)) V' / sqrt(n)) over slots 0..pos[b]
  *   (grouped-query: q-head h reads kv-head h / (Hq/Hkv));

@@ -72,7 +72,7 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
   const uint64_t qd = (uint64_t)s.n_q_heads * s.head_dim;
   uint64_t off = 0;
   L.err = off; off = align256(off + 16);
-  L.qrot = off; off = align256(off + B * qd * 2);
+  L.qrot = off; off = align256(off + B * qd * 4);
   L.o = off; off = align256(off + B * qd * 2);
   L.h = off; off = align256(off + B * s.hidden * 2);
   L.a = off; off = align256(off + B * s.inter * 2);
@@ -151,7 +151,7 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
   int* err = at<int>(base, ws->off_err);
   unsigned* cnt = at<unsigned>(base, ws->off_cnt);
   float* part = at<float>(base, ws->off_part);
-  __half* qrot = at<__half>(base, ws->off_qrot);
+  float* qrot = at<float>(base, ws->off_qrot);
   __nv_bfloat16* o = at<__nv_bfloat16>(base, ws->off_o);
   __nv_bfloat16* h = at<__nv_bfloat16>(base, ws->off_h);
   __nv_bfloat16* a = at<__nv_bfloat16>(base, ws->off_a);

@@ -10,7 +10,8 @@
 // One CTA = (sequence b, kv-head, chunk of CH positions); 4 warps take the
 // chunk's 16-position tiles in turn.  Per tile a warp runs
 //   S = q' K^T: mma.m16n8k16 f16, A = the G query heads of this kv-head
-//     (rows >= G are zero), B = key codes converted in registers (exact);
+//     (rows >= G are zero) as an fp16 pair hi + lo of the fp32 query (two
+//     MMAs), B = key codes converted in registers (exact);
 //     score = S * key_scale * log2(e)/sqrt(d);
 //   online softmax in fp32 (running max m, normalizer l, output rescale);
 //   O += P V: A = fp16(p * value_scale) straight from the score registers,
@@ -77,17 +78,23 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a)
     bulk_g2s(vsc, strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb, &bar);
   }
 
-  // query fragments (A operand of q.k): rows = heads of this group, padded to 16
-  uint32_t qa[D / 16][4];
+  // query fragments (A operand of q.k): rows = heads of this group, padded to
+  // 16; each fp32 pair becomes fp16 hi + lo registers
+  uint32_t qa[D / 16][4], ql[D / 16][4];
   {
-    const __half* q = a.qrot + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
+    const float* q = a.qrot + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
+    const float2 zero = make_float2(0.f, 0.f);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const int c = 16 * ks + 2 * t;
-      qa[ks][0] = g < G ? *reinterpret_cast<const uint32_t*>(q + g * D + c) : 0u;
-      qa[ks][1] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(q + (g + 8) * D + c) : 0u;
-      qa[ks][2] = g < G ? *reinterpret_cast<const uint32_t*>(q + g * D + c + 8) : 0u;
-      qa[ks][3] = g + 8 < G ? *reinterpret_cast<const uint32_t*>(q + (g + 8) * D + c + 8) : 0u;
+      const float2 f0 = g < G ? *reinterpret_cast<const float2*>(q + g * D + c) : zero;
+      const float2 f1 = g + 8 < G ? *reinterpret_cast<const float2*>(q + (g + 8) * D + c) : zero;
+      const float2 f2 = g < G ? *reinterpret_cast<const float2*>(q + g * D + c + 8) : zero;
+      const float2 f3 = g + 8 < G ? *reinterpret_cast<const float2*>(q + (g + 8) * D + c + 8) : zero;
+      split_half2(f0.x, f0.y, qa[ks][0], ql[ks][0]);
+      split_half2(f1.x, f1.y, qa[ks][1], ql[ks][1]);
+      split_half2(f2.x, f2.y, qa[ks][2], ql[ks][2]);
+      split_half2(f3.x, f3.y, qa[ks][3], ql[ks][3]);
     }
   }
   const bool ok = mbar_wait_until(&bar, 0, global_ns() + kWaitNs);
@@ -113,8 +120,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a)
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
         const uint32_t w = kw[j];
-        mma_f16_16816(s[h], qa[2 * j], nib_f16x2(w, 0), nib_f16x2(w, 1));
-        mma_f16_16816(s[h], qa[2 * j + 1], nib_f16x2(w, 2), nib_f16x2(w, 3));
+        const uint32_t k0 = nib_f16x2(w, 0), k1 = nib_f16x2(w, 1), k2 = nib_f16x2(w, 2), k3 = nib_f16x2(w, 3);
+        mma_f16_16816(s[h], qa[2 * j], k0, k1);
+        mma_f16_16816(s[h], qa[2 * j + 1], k2, k3);
+        mma_f16_16816(s[h], ql[2 * j], k0, k1);
+        mma_f16_16816(s[h], ql[2 * j + 1], k2, k3);
       }
     }
     float sc[2][4], vsv[2][2];

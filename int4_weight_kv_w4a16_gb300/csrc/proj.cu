@@ -24,7 +24,7 @@
 //     RESID : out = bf16(resid + acc)                      (O, down)
 //     SWIGLU: a = bf16(silu(r g) * (r u)), r = rms factor  (gate/up rows
 //             interleaved 64/64 per row block)
-//     QKV   : r * acc, RoPE(q, k) at pos, fp32 Hadamard rotation; q -> fp16
+//     QKV   : r * acc, RoPE(q, k) at pos, fp32 Hadamard rotation; q -> fp32
 //             rotated query; k, v -> INT4 + fp16 scale into cache slot pos
 //             (direct KV-cache placement, abstract).
 #include "futr_internal.cuh"
@@ -64,9 +64,9 @@ __device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, in
   }
   warp_fwht<J>(v, a.nh, a.had_c);
   if (is_q) {
-    __half* q = a.qrot + ((size_t)n * a.Hq + hg) * d;
+    float* q = a.qrot + ((size_t)n * a.Hq + hg) * d;
 #pragma unroll
-    for (int j = 0; j < J; ++j) q[lane + 32 * j] = __float2half_rn(v[j]);
+    for (int j = 0; j < J; ++j) q[lane + 32 * j] = v[j];
     return;
   }
   int code[J];

@@ -29,7 +29,7 @@ struct ProjArgs {
   int out_ld;
   // QKV
   const uint64_t* blob_magic;
-  __half* qrot;                  // [batch][Hq][d]
+  float* qrot;                   // [batch][Hq][d] rotated query, fp32
   KvView kv;
   const int* pos;
   const float2* rope;            // [cap][d/2]
@@ -48,7 +48,7 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
 cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream_t st, bool pdl);
 
 struct AttnArgs {
-  const __half* qrot;            // [batch][Hq][d]
+  const float* qrot;             // [batch][Hq][d] rotated query, fp32
   KvView kv;
   const int* pos;
   int batch, Hq, Hkv, G, nh, CH, max_chunks;

@@ -17,10 +17,10 @@ Precision.  Everything is float64 except the two quantizers, whose rounding is
 fixed exactly: scale = fp16(absmax / 7) with the division in fp32, codes =
 round-half-to-even of the fp32 quotient x / fp16 scale, clamped to [-8, 7].
 The fp32 Hadamard butterflies that feed the KV quantizer are emulated in fp32
-in a fixed stage order.  The block evaluation rounds only where the fast path
-stores a narrow type: the rotated query (fp16), the attention output (bf16),
-the residual stream h (bf16), the SwiGLU activation (bf16) and the block output
-(bf16).
+in a fixed stage order.  The block evaluation rounds only where the block's
+activations are stored in bf16 between stages: the attention output o, the
+residual stream h, the SwiGLU activation a and the block output y.  The rotated
+query is kept at full precision.
 
 Readings of points the pages leave open (the plainest one each time):
   * RMSNorm: r = 1/sqrt(mean(x^2) + eps), eps = 1e-5; the gain g_attn is folded
@@ -280,8 +280,8 @@ def stage_qkv(x: np.ndarray, wqkv: np.ndarray, pos: np.ndarray, shape) -> Dict[s
     """RMSNorm (gain already folded), fused QKV projection, RoPE, query rotation.
 
     x: [b, H] float64 (bf16 values); wqkv: dequantized [q_rows + 2 kv_rows, H].
-    Returns q_rot [b, Hq, d] (fp16-rounded), k_new, v_new [b, Hkv, d] (float64,
-    k post-RoPE, both before rotation)."""
+    Returns q_rot [b, Hq, d], k_new, v_new [b, Hkv, d] (float64, k post-RoPE,
+    both before rotation)."""
     b = x.shape[0]
     Hq, Hkv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
     r = rms_factor(x, shape.rms_eps)
@@ -291,7 +291,7 @@ def stage_qkv(x: np.ndarray, wqkv: np.ndarray, pos: np.ndarray, shape) -> Dict[s
     v = qkv[:, (Hq + Hkv) * d:].reshape(b, Hkv, d)
     q = rope(q, pos, shape.rope_theta)
     k = rope(k, pos, shape.rope_theta)
-    q_rot = round_fp16(rotate(q, shape.had_block))
+    q_rot = rotate(q, shape.had_block)
     return {"q_rot": q_rot, "k_new": k, "v_new": v}
 
 

@@ -107,7 +107,7 @@ def block(x, w, cache, pos, sh):
     v = [qkv[(Hq + Hkv + h) * d:(Hq + Hkv + h + 1) * d] for h in range(Hkv)]
     q = [rope(a, pos, sh.rope_theta) for a in q]
     k = [rope(a, pos, sh.rope_theta) for a in k]
-    q_rot = [[f16(a) for a in rotate(qh, n)] for qh in q]
+    q_rot = [rotate(qh, n) for qh in q]
     k_new = [quant(fwht_f32(kh, n)) for kh in k]
     v_new = [quant(fwht_f32(vh, n)) for vh in v]
     o = []

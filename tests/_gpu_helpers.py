@@ -137,7 +137,7 @@ class GpuBlock:
     def intermediates(self, b: int) -> dict:
         s = self.shape
         return {
-            "q_rot": futr.ws_view(self.ws, "qrot", (b, s.n_q_heads, s.head_dim), torch.float16)
+            "q_rot": futr.ws_view(self.ws, "qrot", (b, s.n_q_heads, s.head_dim), torch.float32)
             .cpu().numpy().astype(np.float64),
             "o": bits_to_f64(futr.ws_view(self.ws, "o", (b, s.q_rows), torch.int16)),
             "h": bits_to_f64(futr.ws_view(self.ws, "h", (b, s.hidden), torch.int16)),
