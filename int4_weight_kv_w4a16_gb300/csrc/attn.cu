@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a)
   float* cm = reinterpret_cast<float*>(vsc + CH);  // [warps][G]
   float* cl = cm + kAttnWarps * G;                  // [warps][G]
   float* co = cl + kAttnWarps * G;                  // [warps][G][D]
-  float* mo = co + kAttnWarps * G * D;              // merged [G] m, [G] l, [G][D] O
+  float* mo = co + kAttnWarps * G * D;              // merged [G][D] O, [G] m, [G] l (16-B aligned)
 
   const uint8_t* strm = a.kv.stream(b, kvh);
   if (tid == 0) {
@@ -215,9 +215,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a)
     }
   }
   __syncthreads();
-  float* mm = mo;
-  float* ml = mo + G;
-  float* mO = mo + 2 * G;
+  float* mO = mo;
+  float* mm = mo + G * D;
+  float* ml = mm + G;
   for (int e = tid; e < G * D; e += kAttnWarps * 32) {
     const int r = e / D, i = e % D;
     float M = -INFINITY;
@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a)
     float* wl = co + n_chunks * G;    // [n_chunks][G] l
     for (int i = tid; i < n_chunks * G; i += kAttnWarps * 32) {
       const float* rc = a.apart + rec_base + (size_t)(i / G) * a.rec_floats;
-      wm[i] = __ldcg(rc + i % G);
-      wl[i] = __ldcg(rc + G + i % G);
+      wm[i] = __ldcg(rc + G * D + i % G);
+      wl[i] = __ldcg(rc + G * D + G + i % G);
     }
     __syncthreads();
     if (tid < G) {
@@ -272,21 +272,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnArgs a)
       ml[tid] = Lr;
     }
     __syncthreads();
-    // one element per thread per pass; the chunk loads of a pass are
-    // independent (8 in flight)
-    for (int e = tid; e < G * D; e += kAttnWarps * 32) {
-      const int r = e / D;
-      float Or = 0.f;
+    // four consecutive elements per thread (float4); 8 chunk loads in flight
+    for (int e4 = tid; e4 < G * D / 4; e4 += kAttnWarps * 32) {
+      const int r = (4 * e4) / D;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* src = a.apart + rec_base + 4 * e4;
       for (int c0 = 0; c0 < n_chunks; c0 += 8) {
-        float v[8];
+        float4 v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          v[j] = c0 + j < n_chunks ? __ldcg(a.apart + rec_base + (size_t)(c0 + j) * a.rec_floats + 2 * G + e) : 0.f;
+          v[j] = c0 + j < n_chunks ? __ldcg(reinterpret_cast<const float4*>(src + (size_t)(c0 + j) * a.rec_floats))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (c0 + j < n_chunks) Or += v[j] * wm[(c0 + j) * G + r];
+        for (int j = 0; j < 8; ++j) {
+          const float wt = c0 + j < n_chunks ? wm[(c0 + j) * G + r] : 0.f;
+          acc.x += v[j].x * wt; acc.y += v[j].y * wt; acc.z += v[j].z * wt; acc.w += v[j].w * wt;
+        }
       }
-      mO[e] = Or;
+      reinterpret_cast<float4*>(mO)[e4] = acc;
     }
     if (tid == 0) a.cnt[b * a.Hkv + kvh] = 0u;
     __syncthreads();
@@ -313,6 +316,9 @@ cudaError_t launch_d(const AttnPlan& p, const AttnArgs& a, cudaStream_t st, bool
   if (!(configured & (1ull << (dev & 63)))) {
     cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     configured |= 1ull << (dev & 63);
   }
   cudaLaunchConfig_t cfg = {};
@@ -336,6 +342,8 @@ AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int f
   int ch = 64;
   while (ch < 512 && (long long)batch * s.n_kv_heads * ((cap + ch - 1) / ch) > 8LL * n_sm) ch *= 2;
   if (force_chunk > 0) ch = force_chunk;
+  // the last CTA keeps (m, l) of every chunk in 4*G*D floats of shared memory
+  while ((cap + ch - 1) / ch > 2 * D) ch *= 2;
   p.CH = ch;
   p.max_chunks = (cap + ch - 1) / ch;
   p.rec_floats = (G * (D + 2) + 3) & ~3;

@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
       a.out[(size_t)n * a.out_ld + (size_t)rb * 64 + r] = __float2bfloat16_rn(sg * u);
     }
   } else {
-    if (rb == 0 && sk == 0 && tid == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
+    if (rb == 0 && tid == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
       set_err(a.err, FUTR_ERR_BAD_BLOB);
     const int hpr = kRowsPerBlock / a.d;
     for (int task = warp; task < a.batch * hpr; task += kCW) {
@@ -340,6 +340,11 @@ cudaError_t launch_one(const ProjArgs& a, int grid, size_t smem, cudaStream_t st
   if (!(configured & (1ull << (dev & 63)))) {
     cudaError_t e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kProjMaxSmem);
+    if (e != cudaSuccess) return e;
+    // every kernel of the step asks for the maximum shared-memory carveout, so
+    // CTAs of consecutive kernels can share an SM (programmatic overlap)
+    e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     configured |= 1ull << (dev & 63);
   }

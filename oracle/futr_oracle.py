@@ -296,12 +296,13 @@ def stage_qkv(x: np.ndarray, wqkv: np.ndarray, pos: np.ndarray, shape) -> Dict[s
 
 
 def stage_attention(q_rot: np.ndarray, k_cache: Sequence[np.ndarray], v_cache: Sequence[np.ndarray],
-                    shape) -> np.ndarray:
+                    shape, rnd=None) -> np.ndarray:
     """Single-query GQA attention over the rotated, dequantized cache.
 
     q_rot [b, Hq, d]; k_cache[b], v_cache[b]: [Hkv, L_b, d] (rotated, dequantized,
     the new token included).  The output of every head is rotated back and
-    rounded to bf16: o [b, Hq * d]."""
+    rounded to bf16: o [b, Hq * d].  `rnd` replaces the bf16 rounding
+    (default round_bf16) for callers that choose among tied roundings."""
     b = q_rot.shape[0]
     Hq, Hkv, d = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
     rep = Hq // Hkv
@@ -311,29 +312,29 @@ def stage_attention(q_rot: np.ndarray, k_cache: Sequence[np.ndarray], v_cache: S
             kv = h // rep
             o[i, h] = softmax_attention(q_rot[i, h], k_cache[i][kv], v_cache[i][kv], 1.0 / math.sqrt(d))
     o = rotate(o, shape.had_block)
-    return round_bf16(o.reshape(b, Hq * d))
+    return (rnd or round_bf16)(o.reshape(b, Hq * d))
 
 
-def stage_o(x: np.ndarray, o: np.ndarray, wo: np.ndarray) -> np.ndarray:
+def stage_o(x: np.ndarray, o: np.ndarray, wo: np.ndarray, rnd=None) -> np.ndarray:
     """h = bf16(x + Wo o)."""
-    return round_bf16(x + o @ wo.T)
+    return (rnd or round_bf16)(x + o @ wo.T)
 
 
 def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
-def stage_mlp_in(h: np.ndarray, wgate: np.ndarray, wup: np.ndarray, eps: float) -> np.ndarray:
+def stage_mlp_in(h: np.ndarray, wgate: np.ndarray, wup: np.ndarray, eps: float, rnd=None) -> np.ndarray:
     """RMSNorm (gain folded), gate/up projections, SwiGLU: a = bf16(silu(g) * u)."""
     r = rms_factor(h, eps)[:, None]
     g = r * (h @ wgate.T)
     u = r * (h @ wup.T)
-    return round_bf16(silu(g) * u)
+    return (rnd or round_bf16)(silu(g) * u)
 
 
-def stage_down(h: np.ndarray, a: np.ndarray, wdown: np.ndarray) -> np.ndarray:
+def stage_down(h: np.ndarray, a: np.ndarray, wdown: np.ndarray, rnd=None) -> np.ndarray:
     """y = bf16(h + Wdown a)."""
-    return round_bf16(h + a @ wdown.T)
+    return (rnd or round_bf16)(h + a @ wdown.T)
 
 
 def new_kv_codes(k_new: np.ndarray, v_new: np.ndarray, shape):
