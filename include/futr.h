@@ -225,6 +225,33 @@ futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, con
                                    int32_t layer, int32_t batch, const int32_t* pos_host,
                                    uint16_t* y_host, const futr_ws* ws, void* stream);
 
+/*
+ * futr_decode_block without a caller workspace, for callers that cannot
+ * allocate device memory (a plugin inside a runtime that owns every
+ * allocation, code under a fixed allocator or memory budget, or a program
+ * that must not call cudaMalloc at run time).  The paper has no counterpart:
+ * this is a deployment variant of the same step.  Arguments as for
+ * futr_decode_block; x, blob, kv, pos and y are still the caller's.
+ *
+ * All scratch memory (intermediate activations, partial sums, counters) is a
+ * 16 MiB array inside the library that every device loading the library keeps
+ * until exit.  The call allocates nothing and calls no allocating routine.
+ * - Returns FUTR_ERR_UNSUPPORTED, launching nothing, when this shape, batch and
+ *   the cache's capacity need more than 16 MiB of scratch (an 8B-shaped block
+ *   fits at batch <= 8 with a few thousand cached positions).
+ * - The first call on a device resolves the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ * - Every call uses the same array and clears its counters first, so calls
+ *   whose work overlaps on the GPU (other streams, other threads) race;
+ *   serialize them.
+ * - Device-detected errors land in the array's error word, which the next
+ *   call clears; use futr_decode_block and futr_check when they must be read.
+ */
+futr_status futr_decode_block_noalloc(const uint16_t* x, const void* blob, const futr_kv* kv,
+                                      int32_t layer, int32_t batch, const int32_t* pos, uint16_t* y,
+                                      void* stream);
+
 /* Synchronize `stream`, then return (and clear) the first nonzero device error
  * word of the workspace `ws` and of the cache `kv` (either may be NULL), or
  * FUTR_ERR_CUDA if a CUDA error is pending. */

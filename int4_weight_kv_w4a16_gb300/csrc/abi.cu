@@ -485,3 +485,53 @@ futr_status futr_check(const futr_ws* ws, const futr_kv* kv, void* stream) {
 }
 
 }  // extern "C"
+
+// Helpers for entry points defined in other files of the library.
+namespace futr {
+namespace host {
+
+uint64_t workspace_bytes(const futr_shape& s, int max_batch, int capacity, int n_sm) {
+  return ws_layout(s, max_batch, round16(capacity), n_sm).total;
+}
+
+// Describe a workspace of `bytes` at device address `base` without touching it.
+void describe_workspace(const futr_shape& s, int max_batch, int capacity, int n_sm, void* base, futr_ws* d) {
+  const int cap = round16(capacity);
+  const WsLayout L = ws_layout(s, max_batch, cap, n_sm);
+  *d = futr_ws{};
+  d->shape = s;
+  d->max_batch = max_batch;
+  d->capacity = cap;
+  d->n_sm = n_sm;
+  d->base = base;
+  d->bytes = L.total;
+  d->off_err = L.err;
+  d->off_qrot = L.qrot;
+  d->off_o = L.o;
+  d->off_h = L.h;
+  d->off_a = L.a;
+  d->off_xin = L.xin;
+  d->off_yout = L.yout;
+  d->off_pos = L.pos;
+  d->off_part = L.part;
+  d->part_bytes = L.part_bytes;
+  d->off_apart = L.apart;
+  d->apart_bytes = L.apart_bytes;
+  d->off_cnt = L.cnt;
+  d->cnt_words = L.cnt_words;
+  d->magic = kWsMagic;
+}
+
+int sm_count() { return current_sm_count(); }
+
+futr_status check_decode_args(const void* blob, const futr_kv* kv, int layer, int batch, const futr_ws* ws) {
+  return check_decode(blob, kv, layer, batch, ws);
+}
+
+futr_status launch_block(const uint16_t* x, const void* blob, const futr_kv* kv, int layer, int batch,
+                         const int32_t* pos, uint16_t* y, const futr_ws* ws, cudaStream_t st) {
+  return run_block(x, blob, kv, layer, batch, pos, y, ws, st, nullptr);
+}
+
+}  // namespace host
+}  // namespace futr

@@ -75,6 +75,7 @@ _SIGS = {
                                       C.POINTER(C.c_float)]),
     "futr_decode_block_host": (I32, [P, P, C.POINTER(futr_kv), I32, I32, P, P, C.POINTER(futr_ws), P]),
     "futr_check": (I32, [C.POINTER(futr_ws), C.POINTER(futr_kv), P]),
+    "futr_decode_block_noalloc": (I32, [P, P, C.POINTER(futr_kv), I32, I32, P, P, P]),
 }
 
 
@@ -204,6 +205,13 @@ def futr_decode_block_timed(x, blob, kv, layer, batch, pos, y, ws, stream=None) 
 def futr_decode_block_host(x_host, blob, kv, layer, batch, pos_host, y_host, ws, stream=None):
     _ok(lib().futr_decode_block_host(_ptr(x_host), _ptr(blob), C.byref(kv), layer, batch, _ptr(pos_host),
                                      _ptr(y_host), C.byref(ws), _stream(stream)), "futr_decode_block_host")
+
+
+def futr_decode_block_noalloc(x, blob, kv, layer, batch, pos, y, stream=None):
+    """futr_decode_block with the library's fixed scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _ok(lib().futr_decode_block_noalloc(_ptr(x), _ptr(blob), C.byref(kv), layer, batch, _ptr(pos), _ptr(y),
+                                        _stream(stream)), "futr_decode_block_noalloc")
 
 
 def futr_check(ws=None, kv=None, stream=None) -> int:

@@ -1,0 +1,52 @@
+"""futr_decode_block_noalloc: the decode step for callers that cannot
+allocate device memory, using the library's fixed scratch array.
+
+Its output must match futr_decode_block (caller workspace) on the same
+inputs, on two calls in a row (the second call runs on whatever the first
+left in the shared array).  Collected last on purpose.
+"""
+import numpy as np
+import pytest
+import torch
+
+from int4_weight_kv_w4a16_gb300 import futr, inputs
+from int4_weight_kv_w4a16_gb300.inputs import LLAMA8B, LLAMA70B, TOY
+from tests._gpu_helpers import GpuBlock, assert_close, bits_to_f64, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(shape, lengths, seed):
+    batch = len(lengths)
+    gpu = GpuBlock(shape, inputs.block_weights(shape, seed), max_batch=batch, capacity=max(lengths) + 16)
+    gpu.append_history(0, inputs.kv_history(shape, lengths, seed=seed))
+    x = dev(inputs.activations(shape, batch, seed).view(np.int16))
+    pos = dev(np.asarray(lengths, np.int32))
+    return gpu, x, pos
+
+
+@pytest.mark.parametrize("shape,lengths", [(TOY, [5, 130, 0]), (LLAMA8B, [1024])], ids=["toy_b3", "8b_b1"])
+def test_no_alloc_matches_workspace_entry(shape, lengths):
+    gpu, x, pos = _case(shape, lengths, seed=11)
+    b = len(lengths)
+    y_ref = torch.empty_like(x)
+    futr.futr_decode_block(x, gpu.blob, gpu.kv, 0, b, pos, y_ref, gpu.ws)
+    assert futr.futr_check(gpu.ws, gpu.kv) == 0
+    ref = bits_to_f64(y_ref)
+    for _ in range(2):  # the same cache slot is rewritten with the same token
+        y = torch.zeros_like(x)
+        futr.futr_decode_block_noalloc(x, gpu.blob, gpu.kv, 0, b, pos, y)
+        torch.cuda.synchronize()
+        assert_close(bits_to_f64(y), ref, "no-alloc y")
+
+
+def test_no_alloc_rejects_oversized_scratch():
+    cs = futr.make_shape(LLAMA70B)
+    kv = futr.futr_kv_init(cs, 1, 32, 2048, futr.alloc_bytes(futr.futr_kv_size(cs, 1, 32, 2048)))
+    x = torch.zeros((32, LLAMA70B.hidden), dtype=torch.int16, device="cuda")
+    y = torch.empty_like(x)
+    pos = torch.zeros(32, dtype=torch.int32, device="cuda")
+    blob = futr.alloc_bytes(256)
+    st = futr.lib().futr_decode_block_noalloc(x.data_ptr(), blob.data_ptr(), futr.C.byref(kv), 0, 32,
+                                              pos.data_ptr(), y.data_ptr(), None)
+    assert st == futr.FUTR_ERR_UNSUPPORTED
