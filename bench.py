@@ -81,6 +81,22 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or
+    None when it was taken on another workload or the kernel's sources have
+    changed since."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("workload") != workload:
+        return None
+    h = hashlib.sha256(b"".join(open(os.path.join(ROOT, f), "rb").read() for f in rec["kernel_sources"]))
+    return int(rec["dram_bytes_per_launch"]) if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+
+
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -142,6 +158,13 @@ def max_over_ranks(value: float, world: int) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_us_per_step(ms_max: float, steps: int, world: int) -> float:
+    """Whole-job µs per block-step: every rank runs `steps` block-steps of its
+    own replica in parallel, so N ranks finish N*steps block-steps in the
+    slowest rank's time."""
+    return 1000.0 * ms_max / (steps * world)
 
 
 def barrier(world: int):
@@ -297,7 +320,7 @@ def run_futr(args, wl):
         raise RuntimeError(B.futr.futr_status_string(st))
     ms = max_over_ranks(ms, world)
     us_step = 1000.0 * ms / args.steps
-    value = us_step / world  # whole-job µs per block-step (replicas in parallel)
+    value = whole_job_us_per_step(ms, args.steps, world)
     stage_ms = B.stage_times(min(args.steps, 30))
     pk = peaks()
     total_bytes = sum(B.bytes.values())
@@ -323,7 +346,8 @@ def run_futr(args, wl):
                            "unit": "GB/s", "frac": round(total_bytes / (us_step * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
                            "peak_source": pk["source"]},
         "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(dom_gbs / pk["hbm_gbs"], 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(dom_gbs / pk["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(dom_name, wl.name),
                      "algorithmic_bytes": int(B.bytes[dom_name]), "avg_launch_us": round(stage_ms[dom] * 1e3, 3),
                      "peak_source": pk["source"]},
         "stage_us": {n: round(float(t) * 1e3, 3) for n, t in zip(STAGES, stage_ms)},
