@@ -57,7 +57,8 @@ Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
   const BlobSections sec = blob_sections(s);
   const int force = env_int("FUTR_SPLITK");
   Plans p;
-  for (int i = 0; i < 4; ++i) p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force);
+  const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
+  for (int i = 0; i < 4; ++i) p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
   p.attn = plan_attention(s, batch, cap, n_sm, env_int("FUTR_CHUNK"));
   return p;
 }

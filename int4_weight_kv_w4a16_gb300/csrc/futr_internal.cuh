@@ -176,18 +176,18 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_r
 // Nibble pair (bits 4i and 16+4i of w, offset-8 codes) -> exact bf16x2 codes:
 // 0x4300 | u is the bf16 value 128 + u; subtracting 136 leaves u - 8.
 __device__ __forceinline__ uint32_t nib_bf16x2(uint32_t w, int i) {
-  uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&t);
-  v = __hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f));
-  return *reinterpret_cast<uint32_t*>(&v);
+  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+  uint32_t r;  // 136 = bf16 0x4308; the difference is exact
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
+  return r;
 }
 
 // Same for fp16: 0x6400 | u is 1024 + u; subtracting 1032 leaves u - 8.
 __device__ __forceinline__ uint32_t nib_f16x2(uint32_t w, int i) {
-  uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-  __half2 v = *reinterpret_cast<__half2*>(&t);
-  v = __hsub2(v, __floats2half2_rn(1032.0f, 1032.0f));
-  return *reinterpret_cast<uint32_t*>(&v);
+  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+  uint32_t r;  // 1032 = fp16 0x6408; the difference is exact
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64086408u));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {

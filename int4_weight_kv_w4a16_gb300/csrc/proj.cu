@@ -9,18 +9,20 @@
 // fp32 partial sum is multiplied by its fp16 scale afterwards.
 //
 // Structure of one CTA (row block of 128 outputs x a K-range of groups):
-//   warp 8 (producer): 1-D bulk copies of 8448-byte units (codes + scales)
-//     into a ring of shared-memory stages, completion tracked by mbarriers;
-//     the first stages are issued before griddepcontrol.wait so that weight
-//     streaming overlaps the previous kernel.  After the wait it also copies
-//     the CTA's activation slice [batch][K-range].
-//   warps 0..7 (consumers): warp w owns rows 16w..16w+15; per group it reads
-//     its 32 bytes of nibbles and two scales, releases the stage, builds the
-//     B fragments with ldmatrix from the activation slice and issues 8*NT mma.
-//   split-K: each CTA writes a partial [batch][128] (+ sum of squares of its
-//     activation slice, for RMSNorm); the last CTA of a row block (arrival
-//     counter, no spinning) adds the partials in fixed order and runs the
-//     epilogue:
+//   warp 4 (producer): per 128-input group, one ring stage of shared memory
+//     receives by 1-D bulk copies (mbarrier completion) the weight unit (codes
+//     + scales, 8448 B) and the matching activation tile (one 256-byte row per
+//     batch row, rows padded to 272 B).  Weight units of the first stages are
+//     issued before griddepcontrol.wait, so weight streaming overlaps the
+//     previous kernel; activation tiles follow the wait.
+//   warps 0..3 (consumers): warp w owns rows 32w..32w+31 (two 16-row MMA
+//     tiles sharing each B fragment); per group it reads its 64 bytes of
+//     nibbles and four scales, builds the B fragments with ldmatrix from the
+//     stage's tile, issues 2*8*NT mma, squares its share of the tile for the
+//     RMSNorm sum of squares and releases the stage.
+//   split-K: each CTA writes a partial [batch][128] (+ that sum of squares);
+//     the last CTA of a row block (arrival counter, no spinning) adds the
+//     partials in fixed order and runs the epilogue:
 //     RESID : out = bf16(resid + acc)                      (O, down)
 //     SWIGLU: a = bf16(silu(r g) * (r u)), r = rms factor  (gate/up rows
 //             interleaved 64/64 per row block)
@@ -34,7 +36,8 @@ namespace futr {
 
 namespace {
 
-constexpr int kCW = 8;                    // consumer warps
+constexpr int kCW = 4;                    // consumer warps
+constexpr int kMT = 2;                    // 16-row MMA tiles per consumer warp
 constexpr int kThreads = (kCW + 1) * 32;  // + producer warp
 
 __device__ __forceinline__ void consumer_sync() {
@@ -83,6 +86,14 @@ __device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, in
     store_v_token<J>(a.kv.stream(n, hg - a.Hq - a.Hkv), a.kv.cap, p, code, s, scratch[warp]);
 }
 
+// Activation tile of group g into a ring stage: one 256-byte bulk copy per
+// batch row, rows kTileLd elements apart.
+__device__ __forceinline__ void issue_tile(const ProjArgs& a, uint8_t* stage, int g, uint64_t* bar) {
+  uint8_t* dst = stage + kUnitBytes;
+  const __nv_bfloat16* src = a.xin + (size_t)g * kGroup;
+  for (int n = 0; n < a.batch; ++n) bulk_g2s(dst + n * (kTileLd * 2), src + (size_t)n * a.K, kGroup * 2, bar);
+}
+
 template <int NT, int EPI>
 __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -90,26 +101,22 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
   const int rb = blockIdx.x / a.S, sk = blockIdx.x - rb * a.S;
   const int g0 = (int)(((long long)sk * a.n_groups) / a.S);
   const int g1 = (int)(((long long)(sk + 1) * a.n_groups) / a.S);
-  const int ng = g1 - g0, krange = ng * kGroup, xstride = krange + 8;
+  const int ng = g1 - g0, R = a.ring;
 
   uint8_t* stages = smem;
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem + a.off_xs);
   float* ss = reinterpret_cast<float*>(smem + a.off_misc);  // [32] sum of squares per batch row
-  float* wsum = ss + 32;                                      // [kCW][32]
-  int* flag = reinterpret_cast<int*>(wsum + kCW * 32);        // [4]
+  int* flag = reinterpret_cast<int*>(ss + 32);                // [4]
   uint64_t* full = reinterpret_cast<uint64_t*>(flag + 4);
-  uint64_t* empty = full + kStages;
-  uint64_t* xbar = empty + kStages;
+  uint64_t* empty = full + kMaxRing;
   float* red = reinterpret_cast<float*>(smem);  // epilogue [NT*8][kRedLd], aliases the stages
 
   if (tid == 0) {
     flag[0] = 0;
     flag[1] = 0;
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < R; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kCW);
     }
-    mbar_init(xbar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -119,24 +126,30 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
   if (warp == kCW) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
-      const int pre = ng < kStages ? ng : kStages;
+      const uint32_t tx = kUnitBytes + (uint32_t)a.batch * kGroup * 2;
+      const int pre = ng < R ? ng : R;
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], kUnitBytes);
-        bulk_g2s(stages + i * kUnitBytes, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[i]);
+        mbar_arrive_expect_tx(&full[i], tx);
+        bulk_g2s(stages + (size_t)i * a.stage_bytes, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[i]);
       }
-      pdl_wait();
+      pdl_wait();  // the activations come from the previous kernel
       const unsigned long long deadline = global_ns() + kWaitNs;
-      mbar_arrive_expect_tx(xbar, (uint32_t)(a.batch * krange * 2));
-      for (int n = 0; n < a.batch; ++n)
-        bulk_g2s(xs + n * xstride, a.xin + (size_t)n * a.K + (size_t)g0 * kGroup, krange * 2, xbar);
-      for (int i = kStages; i < ng; ++i) {
-        const int slot = i % kStages;
-        if (!mbar_wait_until(&empty[slot], ((i / kStages) - 1) & 1, deadline)) {
+      for (int i = 0; i < pre; ++i) issue_tile(a, stages + (size_t)i * a.stage_bytes, g0 + i, &full[i]);
+      int slot = 0;
+      uint32_t phase = 0;
+      for (int i = R; i < ng; ++i) {
+        if (!mbar_wait_until(&empty[slot], phase, deadline)) {
           set_err(a.err, FUTR_ERR_TIMEOUT);
           break;
         }
-        mbar_arrive_expect_tx(&full[slot], kUnitBytes);
-        bulk_g2s(stages + slot * kUnitBytes, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[slot]);
+        uint8_t* st = stages + (size_t)slot * a.stage_bytes;
+        mbar_arrive_expect_tx(&full[slot], tx);
+        bulk_g2s(st, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[slot]);
+        issue_tile(a, st, g0 + i, &full[slot]);
+        if (++slot == R) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
     } else {
       pdl_wait();
@@ -147,83 +160,116 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
   // ----------------------------------------------------------- consumers --
   pdl_wait();
   const unsigned long long deadline = global_ns() + kWaitNs;
-  bool ok = mbar_wait_until(xbar, 0, deadline);
+  bool ok = true;
 
-  if (EPI != kEpiResid) {
-    // sum of squares of this CTA's activation slice, fixed reduction order
-    for (int n = 0; n < a.batch; ++n) {
-      float acc = 0.f;
-      for (int c = tid; c < krange; c += kCW * 32) {
-        const float x = __bfloat162float(xs[n * xstride + c]);
-        acc = fmaf(x, x, acc);
-      }
+  float acc[kMT][NT][4];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) wsum[warp * 32 + n] = acc;
-    }
-  }
-  consumer_sync();
-  if (EPI != kEpiResid && tid < a.batch) {
-    float acc = 0.f;
-    for (int w = 0; w < kCW; ++w) acc += wsum[w * 32 + tid];
-    ss[tid] = acc;
-  }
-
-  float acc[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-
-  const int rt = warp, gr = lane >> 2;
-  // ldmatrix row addresses of this lane: batch row 8nt + (lane & 7), column
-  // block (lane >> 3).  Rows past the batch read row 0 instead: they only feed
-  // MMA columns that are never stored.
-  const __nv_bfloat16* xrow[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int n = 8 * nt + (lane & 7);
-    xrow[nt] = xs + (n < a.batch ? n : 0) * xstride + 8 * (lane >> 3);
-  }
-  for (int i = 0; i < ng; ++i) {
-    const int slot = i % kStages;
-    if (!mbar_wait_until(&full[slot], (i / kStages) & 1, deadline)) {
-      ok = false;
-      break;
-    }
-    const uint8_t* st = stages + slot * kUnitBytes;
-    const uint4* wt = reinterpret_cast<const uint4*>(st + rt * 1024);
-    const uint4 w0 = wt[lane], w1 = wt[32 + lane];
-    const __half* sc = reinterpret_cast<const __half*>(st + kUnitCodeBytes);
-    const float s_lo = __half2float(sc[rt * 16 + gr]), s_hi = __half2float(sc[rt * 16 + gr + 8]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
-
-    float dpart[NT][4];
+  for (int m = 0; m < kMT; ++m)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dpart[nt][e] = 0.f;
-    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      for (int e = 0; e < 4; ++e) acc[m][nt][e] = 0.f;
+
+  const int gr = lane >> 2;
+  // ldmatrix row offsets (elements, within a stage's tile) of this lane: batch
+  // row 8nt + (lane & 7), column block (lane >> 3).  Rows past the batch read
+  // row 0 instead: they only feed MMA columns that are never stored.
+  int xrow[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int n = 8 * nt + (lane & 7);
+    xrow[nt] = (n < a.batch ? n : 0) * kTileLd + 8 * (lane >> 3);
+  }
+  // RMSNorm sum of squares of the activations: per group, consumer thread t
+  // squares the 8 elements of tile row t / 16 + 8p, columns 8 (t % 16) .. +7
+  // (16 lanes of one warp cover a row)
+  const int sq_off = (tid >> 4) * kTileLd + 8 * (tid & 15);
+  float ssq[NT];
+#pragma unroll
+  for (int p = 0; p < NT; ++p) ssq[p] = 0.f;
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int i = 0; i < ng; ++i) {
+    if (!mbar_wait_until(&full[slot], phase, deadline)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* st = stages + (size_t)slot * a.stage_bytes;
+    const __nv_bfloat16* tile = reinterpret_cast<const __nv_bfloat16*>(st + kUnitBytes);
+    // this warp's row tiles kMT*warp .. +kMT-1: 1024 contiguous bytes each
+    const uint4* wt = reinterpret_cast<const uint4*>(st + kMT * warp * 1024);
+    uint32_t words[kMT][8];
+    float s_lo[kMT], s_hi[kMT];
+    const __half* sc = reinterpret_cast<const __half*>(st + kUnitCodeBytes);
+#pragma unroll
+    for (int m = 0; m < kMT; ++m) {
+      const uint4 w0 = wt[64 * m + lane], w1 = wt[64 * m + 32 + lane];
+      words[m][0] = w0.x; words[m][1] = w0.y; words[m][2] = w0.z; words[m][3] = w0.w;
+      words[m][4] = w1.x; words[m][5] = w1.y; words[m][6] = w1.z; words[m][7] = w1.w;
+      const int r0 = (kMT * warp + m) * 16 + gr;
+      s_lo[m] = __half2float(sc[r0]);
+      s_hi[m] = __half2float(sc[r0 + 8]);
+    }
+
+    float dpart[kMT][NT][4];
+#pragma unroll
+    for (int m = 0; m < kMT; ++m)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dpart[m][nt][e] = 0.f;
 #pragma unroll
     for (int kp = 0; kp < 4; ++kp) {
       uint32_t bfr[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) ldmatrix_x4(bfr[nt], xrow[nt] + i * kGroup + 32 * kp);
+      for (int nt = 0; nt < NT; ++nt) ldmatrix_x4(bfr[nt], tile + xrow[nt] + 32 * kp);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t w = words[2 * kp + h];
-        const uint32_t af[4] = {nib_bf16x2(w, 0), nib_bf16x2(w, 1), nib_bf16x2(w, 2), nib_bf16x2(w, 3)};
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(dpart[nt], af, bfr[nt][2 * h], bfr[nt][2 * h + 1]);
-      }
+        for (int m = 0; m < kMT; ++m) {
+          const uint32_t w = words[m][2 * kp + h];
+          const uint32_t af[4] = {nib_bf16x2(w, 0), nib_bf16x2(w, 1), nib_bf16x2(w, 2), nib_bf16x2(w, 3)};
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(dpart[m][nt], af, bfr[nt][2 * h], bfr[nt][2 * h + 1]);
+        }
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      acc[nt][0] = fmaf(s_lo, dpart[nt][0], acc[nt][0]);
-      acc[nt][1] = fmaf(s_lo, dpart[nt][1], acc[nt][1]);
-      acc[nt][2] = fmaf(s_hi, dpart[nt][2], acc[nt][2]);
-      acc[nt][3] = fmaf(s_hi, dpart[nt][3], acc[nt][3]);
+    for (int m = 0; m < kMT; ++m)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        acc[m][nt][0] = fmaf(s_lo[m], dpart[m][nt][0], acc[m][nt][0]);
+        acc[m][nt][1] = fmaf(s_lo[m], dpart[m][nt][1], acc[m][nt][1]);
+        acc[m][nt][2] = fmaf(s_hi[m], dpart[m][nt][2], acc[m][nt][2]);
+        acc[m][nt][3] = fmaf(s_hi[m], dpart[m][nt][3], acc[m][nt][3]);
+      }
+    if (EPI != kEpiResid) {
+#pragma unroll
+      for (int p = 0; p < NT; ++p)
+        if ((tid >> 4) + 8 * p < a.batch) {
+          const uint4 v = *reinterpret_cast<const uint4*>(tile + sq_off + 8 * p * kTileLd);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(u[j] << 16), hi = __uint_as_float(u[j] & 0xffff0000u);
+            ssq[p] = fmaf(lo, lo, fmaf(hi, hi, ssq[p]));
+          }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage
+    if (++slot == R) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  if (EPI != kEpiResid) {
+    // the 16 lanes of a half-warp hold the 16 column blocks of one row
+#pragma unroll
+    for (int p = 0; p < NT; ++p) {
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) ssq[p] += __shfl_xor_sync(0xffffffffu, ssq[p], o);
+      const int n = (tid >> 4) + 8 * p;
+      if ((tid & 15) == 0 && n < a.batch) ss[n] = ssq[p];
     }
   }
   if (!ok) {
@@ -237,12 +283,16 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
   {
     const int t = lane & 3;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int n0 = 8 * nt + 2 * t;
-      red[n0 * kRedLd + 16 * rt + gr] = acc[nt][0];
-      red[(n0 + 1) * kRedLd + 16 * rt + gr] = acc[nt][1];
-      red[n0 * kRedLd + 16 * rt + gr + 8] = acc[nt][2];
-      red[(n0 + 1) * kRedLd + 16 * rt + gr + 8] = acc[nt][3];
+    for (int m = 0; m < kMT; ++m) {
+      const int r0 = (kMT * warp + m) * 16 + gr;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n0 = 8 * nt + 2 * t;
+        red[n0 * kRedLd + r0] = acc[m][nt][0];
+        red[(n0 + 1) * kRedLd + r0] = acc[m][nt][1];
+        red[n0 * kRedLd + r0 + 8] = acc[m][nt][2];
+        red[(n0 + 1) * kRedLd + r0 + 8] = acc[m][nt][3];
+      }
     }
   }
   consumer_sync();
@@ -333,21 +383,28 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
 }
 
 template <int NT, int EPI>
-cudaError_t launch_one(const ProjArgs& a, int grid, size_t smem, cudaStream_t st, bool pdl) {
+cudaError_t configure(int dev) {
   static unsigned long long configured = 0;  // one bit per device
+  if (configured & (1ull << (dev & 63))) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kProjMaxSmem);
+  if (e != cudaSuccess) return e;
+  // every kernel of the step asks for the maximum shared-memory carveout, so
+  // CTAs of consecutive kernels can share an SM (programmatic overlap)
+  e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  configured |= 1ull << (dev & 63);
+  return cudaSuccess;
+}
+
+template <int NT, int EPI>
+cudaError_t launch_one(const ProjArgs& a, int grid, size_t smem, cudaStream_t st, bool pdl) {
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured & (1ull << (dev & 63)))) {
-    cudaError_t e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kProjMaxSmem);
-    if (e != cudaSuccess) return e;
-    // every kernel of the step asks for the maximum shared-memory carveout, so
-    // CTAs of consecutive kernels can share an SM (programmatic overlap)
-    e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    configured |= 1ull << (dev & 63);
-  }
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = configure<NT, EPI>(dev);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
@@ -371,29 +428,64 @@ cudaError_t launch_nt(int nt, const ProjArgs& a, int grid, size_t smem, cudaStre
   }
 }
 
+int resident_ctas(int nt, int epi, size_t smem) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  cudaError_t e = cudaSuccess;
+#define FUTR_OCC(NT_, EPI_)                                                               \
+  if (nt == NT_ && epi == EPI_) {                                                         \
+    e = configure<NT_, EPI_>(dev);                                                        \
+    if (e == cudaSuccess)                                                                 \
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_kernel<NT_, EPI_>, kThreads, smem); \
+  }
+  FUTR_OCC(1, 0) FUTR_OCC(2, 0) FUTR_OCC(3, 0) FUTR_OCC(4, 0)
+  FUTR_OCC(1, 1) FUTR_OCC(2, 1) FUTR_OCC(3, 1) FUTR_OCC(4, 1)
+  FUTR_OCC(1, 2) FUTR_OCC(2, 2) FUTR_OCC(3, 2) FUTR_OCC(4, 2)
+#undef FUTR_OCC
+  return e == cudaSuccess ? n : 0;
+}
+
 }  // namespace
 
-ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_split) {
-  ProjPlan p;
+ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_split, int epi) {
+  ProjPlan p{};
   p.n_rb = rows / kRowsPerBlock;
   p.n_groups = cols / kGroup;
   p.nt = (batch + 7) / 8;
-  // activation slice limit: NT*8 rows of (groups*128 + 8) bf16 within kXsMax bytes
-  const int max_groups = ((kXsMax / (batch * 2)) - 8) / kGroup;
-  const int s_min = (p.n_groups + max_groups - 1) / max_groups;
-  int s = (2 * n_sm + p.n_rb - 1) / p.n_rb;
-  if (force_split > 0) s = force_split;
-  if (s < s_min) s = s_min;
-  if (s > p.n_groups) s = p.n_groups;
-  if (s < 1) s = 1;
-  p.S = s;
-  const int gmax = (p.n_groups + s - 1) / s;
-  p.off_xs = kStages * kUnitBytes;
-  int xs_bytes = ((batch * (gmax * kGroup + 8) * 2) + 127) & ~127;
-  const int red_bytes = p.nt * 8 * kRedLd * 4;  // the epilogue tile aliases stages + slice
-  if (kStages * kUnitBytes + xs_bytes < red_bytes) xs_bytes = red_bytes - kStages * kUnitBytes;
-  p.off_misc = p.off_xs + xs_bytes;
-  p.smem = p.off_misc + (32 + kCW * 32) * 4 + 16 + (2 * kStages + 1) * 8;
+  p.epi = epi;
+  // ring stage = weight unit + activation tile; as deep as lets the target
+  // number of CTAs share an SM (5 up to batch 8, else 3)
+  p.stage_bytes = kUnitBytes + batch * kTileLd * 2;
+  const int misc = 32 * 4 + 16 + 2 * kMaxRing * 8;
+  const int per_sm = batch <= 8 ? 5 : 3;
+  const int budget = 232448 / per_sm - 1024 - misc - 2048;  // per-CTA reserve and static arrays
+  int ring = budget / p.stage_bytes;
+  if (ring > kMaxRing) ring = kMaxRing;
+  if (ring < 2) ring = 2;
+  p.ring = ring;
+  int ring_bytes = ring * p.stage_bytes;
+  const int red_bytes = p.nt * 8 * kRedLd * 4;  // the epilogue tile aliases the ring
+  if (ring_bytes < red_bytes) ring_bytes = red_bytes;
+  p.off_misc = (ring_bytes + 127) & ~127;
+  p.smem = (size_t)p.off_misc + misc;
+  // splits: balance waves of resident CTAs; each extra split costs a partial
+  // write and a share of the reduction
+  const int fit = resident_ctas(p.nt, epi, p.smem);
+  const long long slots = (long long)n_sm * (fit > 0 ? fit : 1);
+  int best_s = 1;
+  double best = 1e30;
+  for (int s = 1; s <= p.n_groups; ++s) {
+    const long long items = (long long)p.n_rb * s;
+    const long long waves = (items + slots - 1) / slots;
+    const int per = (p.n_groups + s - 1) / s;
+    const double cost = (double)waves * (per + 3) * (s > 1 ? 1.1 : 1.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  if (force_split > 0) best_s = force_split < p.n_groups ? force_split : p.n_groups;
+  p.S = best_s;
   p.rec_floats = ((batch * (kRowsPerBlock + 1)) + 3) & ~3;
   p.part_floats = (size_t)p.n_rb * p.S * p.rec_floats;
   return p;
@@ -402,7 +494,8 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
 cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream_t st, bool pdl) {
   a.S = p.S;
   a.n_groups = p.n_groups;
-  a.off_xs = p.off_xs;
+  a.ring = p.ring;
+  a.stage_bytes = p.stage_bytes;
   a.off_misc = p.off_misc;
   a.rec_floats = p.rec_floats;
   const int grid = p.n_rb * p.S;

@@ -5,9 +5,9 @@
 
 namespace futr {
 
-constexpr int kStages = 8;          // bulk-copy ring depth (units of 8448 B)
+constexpr int kMaxRing = 8;         // bulk-copy ring depth (stages)
+constexpr int kTileLd = 136;        // bf16 row of an activation tile in shared memory (128 + pad)
 constexpr int kRedLd = 132;         // fp32 row of the epilogue tile (bank-conflict padding)
-constexpr int kXsMax = 64 * 1024;   // activation slice budget in shared memory
 constexpr int kProjMaxSmem = 200 * 1024;
 
 constexpr int kEpiResid = 0;
@@ -18,7 +18,7 @@ struct ProjArgs {
   const uint8_t* w;              // section base of the packed blob
   const __nv_bfloat16* xin;      // activations [batch][K]
   int K, n_groups, S, batch;
-  int off_xs, off_misc, rec_floats;
+  int ring, stage_bytes, off_misc, rec_floats;
   float* part;                   // split-K partial records [n_rb][S][rec_floats]
   unsigned* cnt;                 // arrival counters [n_rb]
   int* err;
@@ -38,13 +38,13 @@ struct ProjArgs {
 };
 
 struct ProjPlan {
-  int n_rb, n_groups, nt, S;
-  int off_xs, off_misc, rec_floats;
+  int n_rb, n_groups, nt, S, epi;
+  int ring, stage_bytes, off_misc, rec_floats;
   size_t smem;
   size_t part_floats;
 };
 
-ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_split);
+ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_split, int epi);
 cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream_t st, bool pdl);
 
 struct AttnArgs {
