@@ -59,7 +59,7 @@ Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
   Plans p;
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
   for (int i = 0; i < 4; ++i) p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
-  p.attn = plan_attention(s, batch, cap, n_sm, env_int("FUTR_CHUNK"));
+  p.attn = plan_attention(s, batch, cap, n_sm, env_int("FUTR_ATTN_SPLIT"));
   return p;
 }
 
@@ -90,7 +90,7 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
   L.part = off; L.part_bytes = part * 4; off = align256(off + L.part_bytes);
   L.apart = off; L.apart_bytes = apart * 4; off = align256(off + L.apart_bytes);
   const BlobSections sec = blob_sections(s);
-  uint64_t cnt = (uint64_t)max_batch * s.n_kv_heads;
+  uint64_t cnt = 0;  // split-K arrival counters, one per row block of each projection
   for (int i = 0; i < 4; ++i) cnt += sec.rows[i] / kRowsPerBlock;
   L.cnt = off; L.cnt_words = cnt; off = align256(off + cnt * 4);
   L.total = off;
@@ -205,14 +205,11 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     A.nh = s.had_block;
     A.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
     A.had_c = had_c;
-    A.apart = at<float>(base, ws->off_apart);
-    A.cnt = cnt_next;
     A.out = o;
     A.err = err;
     if (events) cudaEventRecord(events[1], st);
     e = launch_attention(P.attn, A, s.head_dim, st, pdl);
     if (e != cudaSuccess) return FUTR_ERR_CUDA;
-    cnt_next += (size_t)ws->max_batch * s.n_kv_heads;
   }
   // S4: O projection + residual
   {

@@ -39,6 +39,9 @@ namespace {
 constexpr int kCW = 4;                    // consumer warps
 constexpr int kMT = 2;                    // 16-row MMA tiles per consumer warp
 constexpr int kThreads = (kCW + 1) * 32;  // + producer warp
+constexpr int kRecCols = kRowsPerBlock / 4 + 1;  // float4 columns per batch row of a split record
+constexpr int kRecLd = 4 * kRecCols;             // floats per batch row of a split record
+static_assert(kCW * 32 == kRowsPerBlock, "one consumer thread per output row");
 
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
@@ -272,6 +275,15 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
       if ((tid & 15) == 0 && n < a.batch) ss[n] = ssq[p];
     }
   }
+  // the residual rows of this block (RESID), loaded now so that their latency
+  // overlaps the split handshake
+  __nv_bfloat16 rres[EPI == kEpiResid ? NT * 8 : 1];
+  if (EPI == kEpiResid) {
+#pragma unroll
+    for (int n = 0; n < NT * 8; ++n)
+      rres[n] = n < a.batch ? a.resid[(size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid]
+                            : __float2bfloat16_rn(0.f);
+  }
   if (!ok) {
     set_err(a.err, FUTR_ERR_TIMEOUT);
     flag[1] = 1;
@@ -298,65 +310,79 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
   consumer_sync();
 
   if (a.S > 1) {
-    // publish this split's partial, then count arrivals; the last CTA reduces
+    // publish this split's partial record: per batch row 32 float4 of sums and
+    // one float4 (sum of squares, 0, 0, 0); then count arrivals
     float* rec = a.part + ((size_t)rb * a.S + sk) * a.rec_floats;
-    for (int e = tid; e < a.batch * 32; e += kCW * 32) {
-      const int n = e >> 5, c4 = e & 31;
-      reinterpret_cast<float4*>(rec + n * kRowsPerBlock)[c4] = reinterpret_cast<const float4*>(red + n * kRedLd)[c4];
+    const int items = a.batch * kRecCols;
+    for (int e = tid; e < items; e += kCW * 32) {
+      const int n = e / kRecCols, c4 = e - kRecCols * n;
+      const float4 v = c4 < 32 ? reinterpret_cast<const float4*>(red + n * kRedLd)[c4]
+                               : make_float4(EPI != kEpiResid ? ss[n] : 0.f, 0.f, 0.f, 0.f);
+      reinterpret_cast<float4*>(rec + n * kRecLd)[c4] = v;
     }
-    if (tid < a.batch) rec[a.batch * kRowsPerBlock + tid] = ss[tid];
-    __threadfence();
     consumer_sync();
-    if (tid == 0) {
-      const unsigned prev = atomicAdd(&a.cnt[rb], 1u);
-      flag[0] = (prev == (unsigned)(a.S - 1)) ? 1 : 0;
-    }
+    if (tid == 0) flag[0] = atom_add_acq_rel_gpu(&a.cnt[rb], 1u) == (unsigned)(a.S - 1) ? 1 : 0;
     consumer_sync();
     if (!flag[0]) return;
-    __threadfence();
-    // add the S partials in split order, 8 independent loads in flight
+    // The last CTA adds the S records.  With few columns (small batch), G
+    // groups of threads each add a contiguous range of splits, all loads of a
+    // range in flight together; the G group sums are then added in group
+    // order.  The order is fixed, so the result is deterministic.
+    const int G = items >= kCW * 32 ? 1 : (kCW * 32) / items;
+    float4* gsum = reinterpret_cast<float4*>(red + NT * 8 * kRedLd);  // [G][items], G > 1 only
     const float* part_rb = a.part + (size_t)rb * a.S * a.rec_floats;
-    for (int e = tid; e < a.batch * 32; e += kCW * 32) {
-      const int n = e >> 5, c4 = e & 31;
+    for (int t = tid; t < G * items; t += kCW * 32) {
+      const int grp = t / items, e = t - grp * items;
+      const int n = e / kRecCols, c4 = e - kRecCols * n;
+      const int s_lo = grp * a.S / G, s_hi = (grp + 1) * a.S / G;
+      const float4* src = reinterpret_cast<const float4*>(part_rb + n * kRecLd) + c4;
       float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < a.S; s0 += 8) {
+      for (int s0 = s_lo; s0 < s_hi; s0 += 8) {
         float4 v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (s0 + j < a.S)
-            v[j] = __ldcg(reinterpret_cast<const float4*>(part_rb + (size_t)(s0 + j) * a.rec_floats +
-                                                          n * kRowsPerBlock) + c4);
+          if (s0 + j < s_hi) v[j] = __ldcg(src + (size_t)(s0 + j) * (a.rec_floats / 4));
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (s0 + j < a.S) {
+          if (s0 + j < s_hi) {
             s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
           }
       }
-      reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4;
-    }
-    if (tid < a.batch) {
-      float s2 = 0.f;
-      for (int s0 = 0; s0 < a.S; s0 += 8) {
-        float v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          v[j] = s0 + j < a.S ? __ldcg(part_rb + (size_t)(s0 + j) * a.rec_floats + a.batch * kRowsPerBlock + tid) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (s0 + j < a.S) s2 += v[j];
+      if (G > 1) {
+        gsum[t] = s4;
+      } else if (c4 < 32) {
+        reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4;
+      } else {
+        ss[n] = s4.x;
       }
-      ss[tid] = s2;
+    }
+    if (G > 1) {
+      consumer_sync();
+      for (int e = tid; e < items; e += kCW * 32) {
+        float4 s4 = gsum[e];
+        for (int grp = 1; grp < G; ++grp) {
+          const float4 v = gsum[grp * items + e];
+          s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
+        }
+        const int n = e / kRecCols, c4 = e - kRecCols * n;
+        if (c4 < 32)
+          reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4;
+        else
+          ss[n] = s4.x;
+      }
     }
     if (tid == 0) a.cnt[rb] = 0u;  // self-reset for the next launch
     consumer_sync();
   }
 
   if (EPI == kEpiResid) {
-    for (int e = tid; e < a.batch * kRowsPerBlock; e += kCW * 32) {
-      const int n = e >> 7, r = e & 127;
-      const size_t o = (size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + r;
-      a.out[o] = __float2bfloat16_rn(__bfloat162float(a.resid[o]) + red[n * kRedLd + r]);
-    }
+    // consumer thread t owns output row t of the block (kCW * 32 == 128)
+#pragma unroll
+    for (int n = 0; n < NT * 8; ++n)
+      if (n < a.batch) {
+        const size_t o = (size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid;
+        a.out[o] = __float2bfloat16_rn(__bfloat162float(rres[n]) + red[n * kRedLd + tid]);
+      }
   } else if (EPI == kEpiSwiglu) {
     for (int e = tid; e < a.batch * 64; e += kCW * 32) {
       const int n = e >> 6, r = e & 63;
@@ -464,7 +490,8 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   if (ring < 2) ring = 2;
   p.ring = ring;
   int ring_bytes = ring * p.stage_bytes;
-  const int red_bytes = p.nt * 8 * kRedLd * 4;  // the epilogue tile aliases the ring
+  // the epilogue tile (+ the split-sum groups of small batches) aliases the ring
+  const int red_bytes = p.nt * 8 * kRedLd * 4 + kCW * 32 * 16;
   if (ring_bytes < red_bytes) ring_bytes = red_bytes;
   p.off_misc = (ring_bytes + 127) & ~127;
   p.smem = (size_t)p.off_misc + misc;
@@ -486,7 +513,7 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   }
   if (force_split > 0) best_s = force_split < p.n_groups ? force_split : p.n_groups;
   p.S = best_s;
-  p.rec_floats = ((batch * (kRowsPerBlock + 1)) + 3) & ~3;
+  p.rec_floats = batch * kRecLd;
   p.part_floats = (size_t)p.n_rb * p.S * p.rec_floats;
   return p;
 }

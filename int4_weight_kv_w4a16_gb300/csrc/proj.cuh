@@ -51,23 +51,20 @@ struct AttnArgs {
   const float* qrot;             // [batch][Hq][d] rotated query, fp32
   KvView kv;
   const int* pos;
-  int batch, Hq, Hkv, G, nh, CH, max_chunks;
+  int batch, Hq, Hkv, G, nh;
   float qk_scale_log2;           // log2(e) / sqrt(d)
   float had_c;
-  float* apart;                  // [batch][Hkv][max_chunks][rec]
-  int rec_floats;
-  unsigned* cnt;                 // [batch][Hkv]
   __nv_bfloat16* out;            // [batch][Hq*d]
   int* err;
 };
 
 struct AttnPlan {
-  int CH, max_chunks, rec_floats;
+  int NC;                        // context ranges (cluster size) per (sequence, kv-head)
   size_t smem;
-  size_t part_floats;
+  size_t part_floats;            // global scratch (none: ranges merge in distributed shared memory)
 };
 
-AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int force_chunk);
+AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int force_split);
 cudaError_t launch_attention(const AttnPlan& p, AttnArgs a, int d, cudaStream_t st, bool pdl);
 
 }  // namespace futr

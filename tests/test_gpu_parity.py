@@ -217,6 +217,32 @@ def test_decode_deterministic_and_splitk_invariant(monkeypatch):
         assert_close(o, outs[0], "split-K", rel=2e-3)
 
 
+def test_decode_attention_split_invariant(monkeypatch):
+    """The context ranges of a (sequence, kv-head) merge in a thread-block
+    cluster: 1, 2, 3 or 4 ranges agree within the block tolerance, and a
+    repeated plan is bit-identical."""
+    shape, batch = TOY, 5
+    lengths = [3, 70, 129, 200, 1]
+    weights = inputs.block_weights(shape, 11)
+    x = inputs.activations(shape, batch, 11)
+    hist = inputs.kv_history(shape, lengths, seed=11)
+    pos = np.array(lengths, np.int32)
+    outs = {}
+    for split in (None, None, "1", "2", "3", "4"):
+        if split is None:
+            monkeypatch.delenv("FUTR_ATTN_SPLIT", raising=False)
+        else:
+            monkeypatch.setenv("FUTR_ATTN_SPLIT", split)
+        gpu = GpuBlock(shape, weights, max_batch=batch, capacity=256)
+        gpu.append_history(0, hist)
+        y = bits_to_f64(gpu.decode(x, pos))
+        if split is None and None in outs:
+            np.testing.assert_array_equal(y, outs[None])
+        outs[split] = y
+    for k, o in outs.items():
+        assert_close(o, outs[None], f"attention ranges {k}", rel=2e-3)
+
+
 def test_decode_x_zero_weights_zero():
     shape = TOY
     w = _tiny_weights(shape)

@@ -41,12 +41,21 @@ def test_no_alloc_matches_workspace_entry(shape, lengths):
 
 
 def test_no_alloc_rejects_oversized_scratch():
-    cs = futr.make_shape(LLAMA70B)
-    kv = futr.futr_kv_init(cs, 1, 32, 2048, futr.alloc_bytes(futr.futr_kv_size(cs, 1, 32, 2048)))
-    x = torch.zeros((32, LLAMA70B.hidden), dtype=torch.int16, device="cuda")
+    """A shape whose workspace exceeds the fixed scratch is refused on the host,
+    before any launch.  The refusal is established first from the workspace
+    size, so the call below can only return the status (its dummy weight
+    blob is never read)."""
+    import dataclasses
+    wide = dataclasses.replace(LLAMA70B, hidden=32768, n_q_heads=256, n_kv_heads=32, inter=131072)
+    cs = futr.make_shape(wide)
+    batch, cap = 32, 64
+    need = futr.futr_workspace_size(cs, batch, cap)
+    assert need > 16 * 2**20, need  # otherwise the call below would run
+    kv = futr.futr_kv_init(cs, 1, batch, cap, futr.alloc_bytes(futr.futr_kv_size(cs, 1, batch, cap)))
+    x = torch.zeros((batch, wide.hidden), dtype=torch.int16, device="cuda")
     y = torch.empty_like(x)
-    pos = torch.zeros(32, dtype=torch.int32, device="cuda")
+    pos = torch.zeros(batch, dtype=torch.int32, device="cuda")
     blob = futr.alloc_bytes(256)
-    st = futr.lib().futr_decode_block_noalloc(x.data_ptr(), blob.data_ptr(), futr.C.byref(kv), 0, 32,
+    st = futr.lib().futr_decode_block_noalloc(x.data_ptr(), blob.data_ptr(), futr.C.byref(kv), 0, batch,
                                               pos.data_ptr(), y.data_ptr(), None)
     assert st == futr.FUTR_ERR_UNSUPPORTED
