@@ -89,7 +89,7 @@ typedef struct futr_ws {
   uint64_t off_pos;      /* int32 [b]                                            */
   uint64_t off_part;     /* fp32 split-K partial sums                            */
   uint64_t part_bytes;
-  uint64_t off_apart;    /* fp32 split-context attention partials                */
+  uint64_t off_apart;    /* reserved: 0 bytes (attention merges on chip)         */
   uint64_t apart_bytes;
   uint64_t off_cnt;      /* uint32 arrival counters (self-resetting)             */
   uint64_t cnt_words;
@@ -237,8 +237,8 @@ futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, con
  * 16 MiB array inside the library that every device loading the library keeps
  * until exit.  The call allocates nothing and calls no allocating routine.
  * - Returns FUTR_ERR_UNSUPPORTED, launching nothing, when this shape, batch and
- *   the cache's capacity need more than 16 MiB of scratch (an 8B-shaped block
- *   fits at batch <= 8 with a few thousand cached positions).
+ *   the cache's capacity need more than 16 MiB of scratch (the 8B- and
+ *   70B-shaped blocks fit at every batch up to 32).
  * - The first call on a device resolves the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture.

@@ -34,7 +34,7 @@ constexpr uint64_t kBlobMagic = 0x3141345754554631ull;         // "1FUTW4A1"
 constexpr uint64_t kKvMagic = 0x31564b3452545546ull;
 constexpr uint64_t kWsMagic = 0x3153573452545546ull;
 constexpr int kMaxBatch = 32;
-constexpr int kMaxCapacity = 65536;  // positions per sequence (chunk-merge scratch bound)
+constexpr int kMaxCapacity = 65536;  // positions per sequence
 
 // KV stream of one (layer, seq, kv-head), capacity C (multiple of 16):
 //   K codes: C/8 tiles of 8 positions x d/2 bytes; in a tile, lane 4*p + t
