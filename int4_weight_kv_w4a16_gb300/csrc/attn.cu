@@ -111,13 +111,28 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
   }
   __syncthreads();
   pdl_trigger();
-  pdl_wait();  // q' and the new token's cache entries come from the previous kernel
+  // pos is an input of the step (the previous kernel does not write it), so the
+  // range is known before the wait; the first tiles are pulled into L2 now
+  // (a prefetch cannot return stale data: the copies after the wait read
+  // through L2, which holds the new token's entries once written)
   const int p = a.pos[b];
   const bool pos_ok = p >= 0 && p < cap;
   const int L = pos_ok ? p + 1 : 0;
   const int T = (L + kTilePos - 1) / kTilePos;
   const int tile0 = (int)((long long)sp * T / NC), ntiles = (int)((long long)(sp + 1) * T / NC) - tile0;
   const uint8_t* strm = a.kv.stream(b, kvh);
+  if (warp == kAttnCW && lane == 0) {
+    for (int i = 0; i < ntiles && i < kAttnRing; ++i) {
+      const int c0 = (tile0 + i) * kTilePos;
+      const int n16 = (min(kTilePos, L - c0) + 15) & ~15;
+      const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
+      l2_prefetch(strm + (size_t)c0 * (D / 2), cb);
+      l2_prefetch(strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), cb);
+      l2_prefetch(strm + (size_t)cap * D + 2 * (size_t)c0, sb);
+      l2_prefetch(strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb);
+    }
+  }
+  pdl_wait();  // q' and the new token's cache entries come from the previous kernel
   bool ok = true;
 
   if (warp == kAttnCW) {

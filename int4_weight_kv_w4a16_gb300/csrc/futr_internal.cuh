@@ -143,6 +143,12 @@ __device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, 
   }
 }
 
+// Pull [src, src + bytes) into L2 (no completion, no destination).  src
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
 // dst, src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -287,9 +293,8 @@ struct KvView {
 // Write the codes (warp-held code[j] of dim lane+32j, codes in [-8,7]) and
 // scale of one token of one kv-head into slot p of a stream.  `scratch`:
 // per-warp shared buffer of d bytes.  K slots are plain stores of whole
-// words; V slots are read-modify-write of the nibbles of position p only, so
-// a caller must not write two positions of the same 16-position tile
-// concurrently from different warps.
+// words; V slots update the nibbles of position p only (an atomic AND then an
+// atomic OR per word), so other positions of the tile are left untouched.
 template <int J>
 __device__ __forceinline__ void store_k_token(uint8_t* strm, int cap, int p, const int (&code)[J],
                                               __half s, int8_t* scratch) {
@@ -335,7 +340,10 @@ __device__ __forceinline__ void store_v_token(uint8_t* strm, int cap, int p, con
     const uint32_t n1 = (uint32_t)((scratch[16 * j + 8 + gr] + 8) & 0xF);
     uint32_t* dst = tile + (4 * gr + t) * (d / 16) + j;
     const uint32_t mask = (0xFu << sh) | (0xFu << (sh + 8));
-    *dst = (*dst & ~mask) | (n0 << sh) | (n1 << (sh + 8));
+    // clear, then set, the nibbles of position p: two reductions on the word
+    // (same thread, same address: applied in program order), no read back
+    atomicAnd(dst, ~mask);
+    atomicOr(dst, (n0 << sh) | (n1 << (sh + 8)));
   }
   if (lane == 0) {
     __half* vs = reinterpret_cast<__half*>(strm + (uint64_t)cap * d + 2ull * cap);

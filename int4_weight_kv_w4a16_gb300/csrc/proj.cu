@@ -47,22 +47,42 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
 }
 
+// Position and RoPE (cos, sin) of one head task, loaded ahead of the split
+// handshake where possible: cs[j] pairs dims lane + 32 j and lane + 32 j + d/2.
+struct HeadPre {
+  int p;
+  float2 cs[2];
+};
+
+__device__ __forceinline__ HeadPre load_head_pre(const ProjArgs& a, int n, int hg) {
+  HeadPre h;
+  h.p = a.pos[n];
+  h.cs[0] = h.cs[1] = make_float2(1.f, 0.f);
+  if (hg < a.Hq + a.Hkv) {  // q and k heads are rotated by position
+    const int lane = threadIdx.x & 31, half = a.d / 2;
+    const int pp = h.p >= 0 && h.p < a.kv.cap ? h.p : 0;
+    h.cs[0] = a.rope[(size_t)pp * half + lane];
+    if (half > 32) h.cs[1] = a.rope[(size_t)pp * half + lane + 32];
+  }
+  return h;
+}
+
 template <int J>
-__device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, int hl, int hg, float r) {
+__device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, int hl, int hg, float r,
+                                  const HeadPre& pre) {
   constexpr int d = 32 * J;
   const int lane = threadIdx.x & 31;
   float v[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) v[j] = red[n * kRedLd + hl * d + lane + 32 * j] * r;
-  const int p = a.pos[n];
+  const int p = pre.p;
   const bool is_q = hg < a.Hq, is_k = !is_q && hg < a.Hq + a.Hkv;
   const bool p_ok = p >= 0 && p < a.kv.cap;
   if (is_q || is_k) {
     // rotate-half RoPE: dims i and i + d/2 (lane-local: element j pairs j + J/2)
-    const int pp = p_ok ? p : 0;
 #pragma unroll
     for (int j = 0; j < J / 2; ++j) {
-      const float2 cs = a.rope[(size_t)pp * (d / 2) + lane + 32 * j];
+      const float2 cs = pre.cs[j];
       const float x1 = v[j], x2 = v[j + J / 2];
       v[j] = x1 * cs.x - x2 * cs.y;
       v[j + J / 2] = x2 * cs.x + x1 * cs.y;
@@ -275,8 +295,14 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
       if ((tid & 15) == 0 && n < a.batch) ss[n] = ssq[p];
     }
   }
-  // the residual rows of this block (RESID), loaded now so that their latency
+  // the residual rows of this block (RESID), the position and RoPE factors of
+  // this warp's first head task (QKV), loaded now so that their latency
   // overlaps the split handshake
+  HeadPre pre0{};
+  if (EPI == kEpiQkv) {
+    const int hpr = kRowsPerBlock / a.d;
+    if (warp < a.batch * hpr) pre0 = load_head_pre(a, warp / hpr, rb * hpr + warp % hpr);
+  }
   __nv_bfloat16 rres[EPI == kEpiResid ? NT * 8 : 1];
   if (EPI == kEpiResid) {
 #pragma unroll
@@ -400,10 +426,11 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
       const int n = task / hpr, hl = task % hpr;
       const int hg = rb * hpr + hl;
       const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(ss[n], (float)a.K) + a.eps));
+      const HeadPre pre = task == warp ? pre0 : load_head_pre(a, n, hg);
       if (a.d == 128)
-        qkv_head_epilogue<4>(a, red, n, hl, hg, rn);
+        qkv_head_epilogue<4>(a, red, n, hl, hg, rn, pre);
       else
-        qkv_head_epilogue<2>(a, red, n, hl, hg, rn);
+        qkv_head_epilogue<2>(a, red, n, hl, hg, rn, pre);
     }
   }
 }
