@@ -231,8 +231,9 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
         const uint32_t qa1[4] = {h1.x, h1.y, h1.z, h1.w}, ql1[4] = {l1q.x, l1q.y, l1q.z, l1q.w};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t w = h == 0 ? kw0[j] : kw1[j];
-          const uint32_t k0 = nib_f16x2(w, 0), k1 = nib_f16x2(w, 1), k2 = nib_f16x2(w, 2), k3 = nib_f16x2(w, 3);
+          uint32_t kk[4];
+          nib4_f16x2(h == 0 ? kw0[j] : kw1[j], kk);
+          const uint32_t k0 = kk[0], k1 = kk[1], k2 = kk[2], k3 = kk[3];
           mma_f16_16816(s[h], qa0, k0, k1);
           mma_f16_16816(s[h], qa1, k2, k3);
           mma_f16_16816(s_lo[h], ql0, k0, k1);
@@ -277,12 +278,16 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
       l1 = l1 * corr1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
       m0 = mn0;
       m1 = mn1;
+      // rescale O only when some row's running max moved (corr = 1 otherwise:
+      // the product would leave O unchanged)
+      if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
 #pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        o[nd][0] *= corr0;
-        o[nd][1] *= corr0;
-        o[nd][2] *= corr1;
-        o[nd][3] *= corr1;
+        for (int nd = 0; nd < D / 8; ++nd) {
+          o[nd][0] *= corr0;
+          o[nd][1] *= corr0;
+          o[nd][2] *= corr1;
+          o[nd][3] *= corr1;
+        }
       }
       // P operand = p * value_scale as an fp16 pair hi + lo (hi = fp16(v),
       // lo = fp16(v - hi)): two MMAs keep ~22 bits of each weight.
@@ -294,8 +299,9 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
       const uint32_t* vw = reinterpret_cast<const uint32_t*>(Vs + (size_t)warp * (8 * D) + lane * (D / 4));
 #pragma unroll
       for (int j = 0; j < D / 16; ++j) {
-        const uint32_t w = vw[j];
-        const uint32_t v0 = nib_f16x2(w, 0), v1 = nib_f16x2(w, 1), v2 = nib_f16x2(w, 2), v3 = nib_f16x2(w, 3);
+        uint32_t vv[4];
+        nib4_f16x2(vw[j], vv);
+        const uint32_t v0 = vv[0], v1 = vv[1], v2 = vv[2], v3 = vv[3];
         mma_f16_16816(o[2 * j], pa, v0, v1);
         mma_f16_16816(o[2 * j + 1], pa, v2, v3);
         mma_f16_16816(o[2 * j], pl, v0, v1);

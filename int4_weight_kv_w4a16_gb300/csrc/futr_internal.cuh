@@ -196,12 +196,17 @@ __device__ __forceinline__ uint32_t nib_bf16x2(uint32_t w, int i) {
   return r;
 }
 
-// Same for fp16: 0x6400 | u is 1024 + u; subtracting 1032 leaves u - 8.
-__device__ __forceinline__ uint32_t nib_f16x2(uint32_t w, int i) {
-  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-  uint32_t r;  // 1032 = fp16 0x6408; the difference is exact
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64086408u));
-  return r;
+// All four fp16x2 registers of a word (slots (i, i+4), i = 0..3) with one
+// shift: fp16 keeps 10 mantissa bits, so a nibble at bits 4-7 of a half is
+// exact too: 0x6400 | u << 4 is 1024 + 16u, and (1024 + 16u) / 16 - 72 = u - 8.
+__device__ __forceinline__ void nib4_f16x2(uint32_t w, uint32_t (&r)[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t t0 = (w & 0x000F000Fu) | 0x64006400u, t1 = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t t2 = (w8 & 0x000F000Fu) | 0x64006400u, t3 = (w8 & 0x00F000F0u) | 0x64006400u;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(0x64086408u));             // - 1032
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[1]) : "r"(t1), "r"(0x2C002C00u), "r"(0xD480D480u));  // / 16 - 72
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[2]) : "r"(t2), "r"(0x64086408u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[3]) : "r"(t3), "r"(0x2C002C00u), "r"(0xD480D480u));
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
