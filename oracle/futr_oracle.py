@@ -34,6 +34,11 @@ Readings of points the pages leave open (the plainest one each time):
   * GQA: query head h reads kv-head h // (n_q_heads / n_kv_heads).
   * pos[b] is the number of tokens already cached; the new token goes to slot
     pos[b] and attention spans positions 0..pos[b].
+  * Full decode step (embedding, the blocks, final RMSNorm, LM head): the LM
+    head stays bf16 (no INT4 projection follows the final norm, so its gain
+    cannot be folded into INT4 codes).  The final gain multiplies the last
+    block's output in fp32 and the product is rounded once to bf16, the LM
+    head's activation; the RMSNorm factor r (float64 here) scales the logits.
 """
 from __future__ import annotations
 
@@ -388,3 +393,45 @@ def build_cache(kv_hist: Sequence[tuple], shape) -> List[dict]:
         vc, vs = kv_quantize(v32, shape.had_block)
         out.append({"k_codes": kc, "k_scales": ks, "v_codes": vc, "v_scales": vs})
     return out
+
+
+# ----------------------------------------------------------- full decode step
+
+def float_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of values that are already exactly bf16."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    assert np.array_equal(f.astype(np.float64), np.asarray(x, dtype=np.float64)), "not bf16-exact"
+    u = f.view(np.uint32)
+    assert not np.any(u & 0xFFFF), "not bf16-exact"
+    return (u >> 16).astype(np.uint16)
+
+
+def embed(tokens: np.ndarray, table_bits: np.ndarray) -> np.ndarray:
+    """x_b = row tokens[b] of the bf16 embedding table (bits [vocab, H]); bits."""
+    return np.asarray(table_bits)[np.asarray(tokens, dtype=np.int64)]
+
+
+def final_logits(y: np.ndarray, g_final: np.ndarray, w_lm_bits: np.ndarray, eps: float) -> np.ndarray:
+    """Final RMSNorm + bf16 LM head: logits[b, v] = r_b * sum_k W[v, k] xg[b, k],
+    r_b = 1/sqrt(mean_k y_bk^2 + eps), xg = bf16(fp32(g_k * y_bk)) (reading: the
+    gain is applied in fp32 to the block output and rounded once to bf16)."""
+    y = np.asarray(y, dtype=np.float64)
+    r = rms_factor(y, eps)
+    xg = round_bf16((y.astype(np.float32) * np.asarray(g_final, dtype=np.float32)).astype(np.float64))
+    w = bf16_bits_to_float(w_lm_bits)
+    return r[:, None] * (xg @ w.T)
+
+
+def decode_step(tokens: np.ndarray, table_bits: np.ndarray, layers: Sequence[Dict[str, np.ndarray]],
+                caches: Sequence[Sequence[dict]], pos: np.ndarray, g_final: np.ndarray, w_lm_bits: np.ndarray,
+                shape, new_kv: Optional[Sequence[tuple]] = None) -> Dict[str, object]:
+    """Embedding, then every block (``decode_block`` with layers[l], caches[l]),
+    then ``final_logits``.  new_kv[l]: optional new-token cache entries per layer
+    (as in ``decode_block``).  Returns the per-layer outputs and the logits."""
+    x_bits = embed(tokens, table_bits)
+    ys = []
+    for l, wdq in enumerate(layers):
+        out = decode_block(x_bits, wdq, caches[l], pos, shape, None if new_kv is None else new_kv[l])
+        ys.append(out["y"])
+        x_bits = float_to_bf16_bits(out["y"])
+    return {"y": ys, "logits": final_logits(ys[-1], g_final, w_lm_bits, shape.rms_eps)}

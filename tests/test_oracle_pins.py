@@ -338,3 +338,78 @@ def test_decode_block_batch_permutation():
     perm = [2, 0, 1]
     b = oracle.decode_block(xb[perm], w, [cache[i] for i in perm], pos[perm], sh)
     np.testing.assert_array_equal(b["y"], a["y"][perm])
+
+
+# -------------------------------------------------------- full decode step --
+
+def _bf16_bits(x) -> np.ndarray:
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_embed_takes_table_rows():
+    table = np.random.default_rng(40).integers(0, 2 ** 16, (37, 8)).astype(np.uint16)
+    tok = np.array([5, 0, 36, 5])
+    np.testing.assert_array_equal(oracle.embed(tok, table), table[[5, 0, 36, 5]])
+
+
+def test_final_logits_unit_gain_is_rmsnorm_then_matmul():
+    # g = 1: bf16(g * y) = y exactly, so the logits are RMSNorm(y) W^T by the
+    # definition, evaluated here with explicit Python sums
+    r = np.random.default_rng(41)
+    H, V, b = 64, 24, 3
+    y = oracle.bf16_bits_to_float(_bf16_bits(r.standard_normal((b, H))))
+    wb = _bf16_bits(r.standard_normal((V, H)) * 0.05)
+    w = oracle.bf16_bits_to_float(wb)
+    got = oracle.final_logits(y, np.ones(H, np.float32), wb, 1e-5)
+    for i in range(b):
+        den = math.sqrt(sum(float(v) * float(v) for v in y[i]) / H + 1e-5)
+        ref = [sum(float(w[v, k]) * float(y[i, k]) for k in range(H)) / den for v in range(V)]
+        np.testing.assert_allclose(got[i], np.array(ref), rtol=1e-12, atol=1e-12)
+
+
+def test_final_logits_gain_rounded_once_to_bf16():
+    # a general gain: the activation is bf16(fp32(g y)); against the unrounded
+    # RMSNorm(y) * g the error per logit is at most r * sum_k |W_vk| |g_k y_k| 2^-8
+    r = np.random.default_rng(42)
+    H, V, b = 128, 40, 2
+    y = oracle.bf16_bits_to_float(_bf16_bits(r.standard_normal((b, H)) * 3))
+    g = r.uniform(0.5, 1.5, H).astype(np.float32)
+    wb = _bf16_bits(r.standard_normal((V, H)) * 0.05)
+    w = oracle.bf16_bits_to_float(wb)
+    got = oracle.final_logits(y, g, wb, 1e-5)
+    rms = np.sqrt(np.mean(y * y, axis=1) + 1e-5)
+    exact = ((y * g.astype(np.float64)) / rms[:, None]) @ w.T
+    bound = (np.abs(y * g.astype(np.float64)) @ np.abs(w).T) / rms[:, None] * 2.0 ** -8
+    assert np.all(np.abs(got - exact) <= bound + 1e-15)
+    assert np.any(got != exact)  # the rounding is there
+
+
+def test_final_logits_reads_rows_of_the_head():
+    # one-hot rows: logit v is r * bf16(g_v y_v); a transposed head or a dropped
+    # factor fails
+    H = 16
+    y = oracle.bf16_bits_to_float(_bf16_bits(np.arange(1, H + 1, dtype=np.float32) / 4))[None, :]
+    w = np.zeros((6, H), np.float32)
+    for v in range(6):
+        w[v, 3 * v % H] = 1.0
+    g = np.full(H, 2.0, np.float32)
+    got = oracle.final_logits(y, g, _bf16_bits(w), 1e-5)[0]
+    r = 1.0 / math.sqrt(float(np.mean(y * y)) + 1e-5)
+    np.testing.assert_allclose(got, [r * 2.0 * y[0, 3 * v % H] for v in range(6)], rtol=1e-15)
+
+
+def test_decode_step_chains_the_blocks():
+    sh = oracle_shape_tiny()
+    w1, _, c1 = _tiny_case(sh, 2, [3, 1], seed=50)
+    w2, _, c2 = _tiny_case(sh, 2, [3, 1], seed=51)
+    r = np.random.default_rng(52)
+    table = _bf16_bits(r.standard_normal((11, sh.hidden)))
+    wlm = _bf16_bits(r.standard_normal((9, sh.hidden)) * 0.05)
+    g = r.uniform(0.5, 1.5, sh.hidden).astype(np.float32)
+    tok, pos = np.array([4, 10]), np.array([3, 1])
+    out = oracle.decode_step(tok, table, [w1, w2], [c1, c2], pos, g, wlm, sh)
+    y1 = oracle.decode_block(table[tok], w1, c1, pos, sh)["y"]
+    y2 = oracle.decode_block(_bf16_bits(y1), w2, c2, pos, sh)["y"]
+    np.testing.assert_array_equal(out["y"][0], y1)
+    np.testing.assert_array_equal(out["y"][1], y2)
+    np.testing.assert_array_equal(out["logits"], oracle.final_logits(y2, g, wlm, sh.rms_eps))
