@@ -252,6 +252,32 @@ futr_status futr_decode_block_noalloc(const uint16_t* x, const void* blob, const
                                       int32_t layer, int32_t batch, const int32_t* pos, uint16_t* y,
                                       void* stream);
 
+/*
+ * One complete decode step of an n_layers-block model: the abstract of
+ * "FuTransformer: FP8 prefill and INT4 decode for Llama-style inference on
+ * Hopper" times a complete Llama-3.1-8B decode step (the blocks plus the
+ * embedding, the final norm and the LM head).
+ *   x = embedding[tokens[b]];  for l < n_layers: x = futr_decode_block(x, blobs[l],
+ *   layer l);  r = 1/sqrt(mean(x^2)+eps);  xg = bf16(fp32(g_final * x));
+ *   logits[b][v] = r * sum_k lm_head[v][k] * xg[k]   (fp32 accumulation).
+ * No INT4 projection follows the final norm, so its gain cannot be folded into
+ * INT4 codes: the LM head stays bf16 and the gain scales the activation.
+ * tokens: device int32 [batch]; a token outside [0, vocab) sets
+ * FUTR_ERR_OUT_OF_RANGE and reads as a zero embedding.  embedding, lm_head:
+ * device bf16 [vocab][H], 16-byte aligned, vocab a multiple of 64.  blobs: HOST
+ * array of n_layers device pointers (packed weights of layers 0..n_layers-1;
+ * kv must hold at least n_layers layers).  pos as for futr_decode_block.
+ * g_final: device fp32 [H].  logits: device fp32 [batch][vocab].  The residual
+ * stream passes through the workspace's staging rows, which the step uses in
+ * place of futr_decode_block_host's.  Launches embedding, 5 kernels per block,
+ * final norm and LM head with programmatic dependent launch; capturable.
+ */
+futr_status futr_decode_step(const int32_t* tokens, const uint16_t* embedding, int32_t vocab,
+                             const void* const* blobs, int32_t n_layers, const futr_kv* kv,
+                             int32_t batch, const int32_t* pos, const float* g_final,
+                             const uint16_t* lm_head, float* logits, const futr_ws* ws,
+                             void* stream);
+
 /* Synchronize `stream`, then return (and clear) the first nonzero device error
  * word of the workspace `ws` and of the cache `kv` (either may be NULL), or
  * FUTR_ERR_CUDA if a CUDA error is pending. */

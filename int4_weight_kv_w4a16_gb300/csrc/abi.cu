@@ -463,6 +463,39 @@ futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, con
   return cuda_status(cudaStreamSynchronize(s));
 }
 
+futr_status futr_decode_step(const int32_t* tokens, const uint16_t* embedding, int32_t vocab,
+                             const void* const* blobs, int32_t n_layers, const futr_kv* kv, int32_t batch,
+                             const int32_t* pos, const float* g_final, const uint16_t* lm_head, float* logits,
+                             const futr_ws* ws, void* stream) {
+  if (!tokens || !embedding || !blobs || !pos || !g_final || !lm_head || !logits) return FUTR_ERR_INVALID_ARG;
+  if (vocab <= 0 || vocab % 64) return FUTR_ERR_UNSUPPORTED;
+  if (n_layers < 1 || !kv_ok(kv) || n_layers > kv->n_layers) return FUTR_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(embedding) & 15) || (reinterpret_cast<uintptr_t>(lm_head) & 15))
+    return FUTR_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const futr_status st = check_decode(blobs[l], kv, l, batch, ws);
+    if (st != FUTR_OK) return st;
+  }
+  const futr_shape& s = ws->shape;
+  const cudaStream_t st = as_stream(stream);
+  void* base = ws->base;
+  int* err = at<int>(base, ws->off_err);
+  // the two staging rows of the workspace carry the residual stream from block
+  // to block; h holds the LM head's activation and q' the norm factors
+  uint16_t* buf[2] = {at<uint16_t>(base, ws->off_xin), at<uint16_t>(base, ws->off_yout)};
+  uint16_t* xg = at<uint16_t>(base, ws->off_h);
+  float* r = at<float>(base, ws->off_qrot);
+  if (launch_embed(tokens, embedding, vocab, s.hidden, batch, buf[0], err, st, true) != cudaSuccess)
+    return FUTR_ERR_CUDA;
+  for (int l = 0; l < n_layers; ++l) {
+    const futr_status e = run_block(buf[l & 1], blobs[l], kv, l, batch, pos, buf[(l + 1) & 1], ws, st, nullptr);
+    if (e != FUTR_OK) return e;
+  }
+  if (launch_final_norm(buf[n_layers & 1], g_final, s.hidden, s.rms_eps, batch, xg, r, st, true) != cudaSuccess)
+    return FUTR_ERR_CUDA;
+  return cuda_status(launch_lm_head(xg, lm_head, vocab, s.hidden, batch, r, logits, err, st, true));
+}
+
 futr_status futr_check(const futr_ws* ws, const futr_kv* kv, void* stream) {
   cudaStream_t s = as_stream(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return FUTR_ERR_CUDA;

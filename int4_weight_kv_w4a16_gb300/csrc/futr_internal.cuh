@@ -370,5 +370,11 @@ cudaError_t launch_kv_append(const futr_kv& kv, int layer, int seq0, int batch, 
 cudaError_t launch_kv_read(const futr_kv& kv, int layer, int seq, int n_pos, int8_t* kc, uint16_t* ks,
                            int8_t* vc, uint16_t* vs, cudaStream_t st);
 KvView kv_layer_view(const futr_kv& kv, int layer);
+cudaError_t launch_embed(const int* tokens, const uint16_t* table, int vocab, int H, int batch, uint16_t* x,
+                         int* err, cudaStream_t st, bool pdl);
+cudaError_t launch_final_norm(const uint16_t* y, const float* g, int H, float eps, int batch, uint16_t* xg, float* r,
+                              cudaStream_t st, bool pdl);
+cudaError_t launch_lm_head(const uint16_t* xg, const uint16_t* w, int vocab, int H, int batch, const float* r,
+                           float* logits, int* err, cudaStream_t st, bool pdl);
 
 }  // namespace futr

@@ -76,6 +76,8 @@ _SIGS = {
     "futr_decode_block_host": (I32, [P, P, C.POINTER(futr_kv), I32, I32, P, P, C.POINTER(futr_ws), P]),
     "futr_check": (I32, [C.POINTER(futr_ws), C.POINTER(futr_kv), P]),
     "futr_decode_block_noalloc": (I32, [P, P, C.POINTER(futr_kv), I32, I32, P, P, P]),
+    "futr_decode_step": (I32, [P, P, I32, C.POINTER(C.c_void_p), I32, C.POINTER(futr_kv), I32, P, P, P, P,
+                               C.POINTER(futr_ws), P]),
 }
 
 
@@ -205,6 +207,15 @@ def futr_decode_block_timed(x, blob, kv, layer, batch, pos, y, ws, stream=None) 
 def futr_decode_block_host(x_host, blob, kv, layer, batch, pos_host, y_host, ws, stream=None):
     _ok(lib().futr_decode_block_host(_ptr(x_host), _ptr(blob), C.byref(kv), layer, batch, _ptr(pos_host),
                                      _ptr(y_host), C.byref(ws), _stream(stream)), "futr_decode_block_host")
+
+
+def futr_decode_step(tokens, embedding, vocab, blobs, kv, batch, pos, g_final, lm_head, logits, ws, stream=None):
+    """One complete decode step (embedding, every block in ``blobs``, final
+    norm, bf16 LM head) -> fp32 logits [batch, vocab]."""
+    arr = (C.c_void_p * len(blobs))(*[_ptr(b) for b in blobs])
+    _ok(lib().futr_decode_step(_ptr(tokens), _ptr(embedding), vocab, arr, len(blobs), C.byref(kv), batch,
+                               _ptr(pos), _ptr(g_final), _ptr(lm_head), _ptr(logits), C.byref(ws),
+                               _stream(stream)), "futr_decode_step")
 
 
 def futr_decode_block_noalloc(x, blob, kv, layer, batch, pos, y, stream=None):

@@ -1,0 +1,140 @@
+"""The full decode step through the C ABI (futr_decode_step): embedding, the
+blocks, final RMSNorm and the bf16 LM head, against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int4_weight_kv_w4a16_gb300 import futr, inputs
+from int4_weight_kv_w4a16_gb300.inputs import LLAMA8B, TOY
+from tests._gpu_helpers import assert_close, dev, ensure_lib
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.bfloat16).cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+class Model:
+    """n_layers packed blocks, one INT4 cache, a workspace, embedding, final
+    gain and LM head on cuda:0."""
+
+    def __init__(self, shape, n_layers, vocab, max_batch, capacity, seed=0, host_weights=True):
+        ensure_lib()
+        self.shape, self.vocab, self.n_layers = shape, vocab, n_layers
+        self.cs = futr.make_shape(shape)
+        self.blobs, self.weights = [], []
+        for l in range(n_layers):
+            w = inputs.block_weights(shape, seed + l)
+            blob = futr.alloc_bytes(futr.futr_weights_size(self.cs))
+            d = {k: dev(v) for k, v in w.items()}
+            futr.futr_pack_weights(self.cs, d["wq"], d["wk"], d["wv"], d["wo"], d["wgate"], d["wup"], d["wdown"],
+                                   d["g_attn"], d["g_mlp"], blob)
+            del d
+            self.blobs.append(blob)
+            self.weights.append(w if host_weights else None)
+        self.kv = futr.futr_kv_init(self.cs, n_layers, max_batch, capacity,
+                                    futr.alloc_bytes(futr.futr_kv_size(self.cs, n_layers, max_batch, capacity)))
+        self.ws = futr.futr_workspace_init(self.cs, max_batch, capacity,
+                                           futr.alloc_bytes(futr.futr_workspace_size(self.cs, max_batch, capacity)))
+        g = torch.Generator(device="cuda").manual_seed(1000 + seed)
+        self.embedding = (torch.randn((vocab, shape.hidden), generator=g, device="cuda")).to(torch.bfloat16)
+        self.lm_head = (torch.randn((vocab, shape.hidden), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+        self.g_final = (torch.rand(shape.hidden, generator=g, device="cuda") + 0.5).float()
+        torch.cuda.synchronize()
+
+    def append_history(self, lengths, seed=0):
+        for l in range(self.n_layers):
+            for b, (kb, vb) in enumerate(inputs.kv_history(self.shape, lengths, seed=seed + 7 * l)):
+                if kb.shape[1]:
+                    futr.futr_kv_append(self.kv, l, b, 1, dev(np.array([0], np.int32)), kb.shape[1], dev(kb), dev(vb))
+
+    def step(self, tokens, pos):
+        b = len(tokens)
+        logits = torch.empty((b, self.vocab), dtype=torch.float32, device="cuda")
+        futr.futr_decode_step(dev(np.asarray(tokens, np.int32)), self.embedding, self.vocab, self.blobs, self.kv, b,
+                              dev(np.asarray(pos, np.int32)), self.g_final, self.lm_head, logits, self.ws)
+        return logits
+
+    def final_hidden(self, b):
+        """The last block's output, left by the step in its staging row."""
+        name = "xin" if self.n_layers % 2 == 0 else "yout"
+        return futr.ws_view(self.ws, name, (b, self.shape.hidden), torch.int16).cpu().numpy().view(np.uint16)
+
+    def read_cache(self, layer, seq, n):
+        Hkv, d = self.shape.n_kv_heads, self.shape.head_dim
+        kc = torch.empty((Hkv, n, d), dtype=torch.int8, device="cuda")
+        vc = torch.empty_like(kc)
+        ks = torch.empty((Hkv, n), dtype=torch.int16, device="cuda")
+        vs = torch.empty_like(ks)
+        futr.futr_kv_read(self.kv, layer, seq, n, kc, ks, vc, vs)
+        return {"k_codes": kc.cpu().numpy(), "k_scales": ks.cpu().numpy().view(np.float16),
+                "v_codes": vc.cpu().numpy(), "v_scales": vs.cpu().numpy().view(np.float16)}
+
+
+def test_step_toy_two_layers_end_to_end():
+    sh, vocab, lengths = TOY, 1024, [5, 70, 0]
+    m = Model(sh, 2, vocab, max_batch=4, capacity=96)
+    m.append_history(lengths)
+    tokens, pos = np.array([3, 1023, 512]), np.array(lengths)
+    logits = m.step(tokens, pos).cpu().numpy().astype(np.float64)
+    assert futr.futr_check(m.ws, m.kv) == 0
+    g = m.g_final.cpu().numpy()
+    wlm = bf16_bits(m.lm_head)
+
+    # final norm + LM head on the GPU's last hidden state (tight: same bf16 activation)
+    y = oracle.bf16_bits_to_float(m.final_hidden(len(tokens)))
+    assert_close(logits, oracle.final_logits(y, g, wlm, sh.rms_eps), "logits from the GPU's hidden state", rel=1e-5,
+                 mx=1e-4)
+
+    # end to end from the tokens, on the identical dequantized weights and
+    # cache (the GPU's entries for the new token of each layer)
+    layers = [oracle.dequant_block(oracle.pack_block(w)) for w in m.weights]
+    caches, new_kv = [], []
+    hist = [inputs.kv_history(sh, lengths, seed=7 * l) for l in range(2)]
+    for l in range(2):
+        caches.append(oracle.build_cache(hist[l], sh))
+        parts = [np.zeros((3, sh.n_kv_heads, sh.head_dim), np.int8), np.zeros((3, sh.n_kv_heads), np.float16),
+                 np.zeros((3, sh.n_kv_heads, sh.head_dim), np.int8), np.zeros((3, sh.n_kv_heads), np.float16)]
+        for i, L in enumerate(lengths):
+            c = m.read_cache(l, i, L + 1)
+            parts[0][i], parts[1][i] = c["k_codes"][:, L], c["k_scales"][:, L]
+            parts[2][i], parts[3][i] = c["v_codes"][:, L], c["v_scales"][:, L]
+        new_kv.append(tuple(parts))
+    ref = oracle.decode_step(tokens, bf16_bits(m.embedding), layers, caches, pos, g, wlm, sh, new_kv=new_kv)
+    assert_close(oracle.bf16_bits_to_float(m.final_hidden(3)), ref["y"][-1], "last hidden state", flip=True)
+    assert_close(logits, ref["logits"], "logits")
+
+
+def test_step_deterministic_and_token_range_flagged():
+    sh, vocab = TOY, 512
+    m = Model(sh, 3, vocab, max_batch=2, capacity=64, seed=3)
+    m.append_history([9, 2], seed=3)
+    a = m.step([7, 9], [9, 2]).cpu().numpy()
+    b = m.step([7, 9], [9, 2]).cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+    assert futr.futr_check(m.ws, m.kv) == 0
+    bad = m.step([7, vocab], [9, 2]).cpu().numpy()  # token past the table
+    assert futr.futr_check(m.ws, m.kv) == futr.FUTR_ERR_OUT_OF_RANGE
+    assert np.all(np.isfinite(bad))
+
+
+@pytest.mark.parametrize("batch", [1, 16])
+def test_step_full_vocabulary_lm_head(batch):
+    """8B-shaped blocks and the full 128256-row head: sampled vocabulary rows
+    against the oracle's final norm + LM head on the GPU's last hidden state."""
+    sh, vocab = LLAMA8B, 128256
+    m = Model(sh, 2, vocab, max_batch=batch, capacity=272, seed=5, host_weights=False)
+    lengths = [256 - 13 * (i % 5) for i in range(batch)]
+    m.append_history(lengths, seed=5)
+    tokens = (np.arange(batch) * 7919 + 11) % vocab
+    logits = m.step(tokens, lengths)
+    assert futr.futr_check(m.ws, m.kv) == 0
+    rows = np.sort(np.random.default_rng(batch).choice(vocab, 256, replace=False))
+    w_rows = bf16_bits(m.lm_head[torch.from_numpy(rows).cuda()])
+    y = oracle.bf16_bits_to_float(m.final_hidden(batch))
+    ref = oracle.final_logits(y, m.g_final.cpu().numpy(), w_rows, sh.rms_eps)
+    got = logits.cpu().numpy().astype(np.float64)[:, rows]
+    assert_close(got, ref, "sampled logits", rel=1e-5, mx=1e-4)
+    assert np.all(np.isfinite(logits.cpu().numpy()))
