@@ -13,6 +13,9 @@ JSON line on stdout (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl futr|reference]
 
+The llama8b_x32_* workloads time the complete model step instead (32 blocks,
+embedding, final norm and bf16 LM head; futr_decode_step, 164 kernels per step).
+
 --impl reference times the float64 CPU oracle on the host cores instead.
 Under torchrun (N > 1) every rank runs an independent replica (no collective
 on the data path); elapsed time is the max over ranks.
@@ -367,6 +370,196 @@ def run_futr(args, wl):
         dist.destroy_process_group()
 
 
+# --------------------------------------------------- complete decode step --
+
+STEP_METRIC = "INT4 decode µs/step, complete 8B model (32 INT4 blocks + embedding + bf16 LM head)"
+STEP_UNIT = "us/step"
+
+
+class StepBench:
+    """The complete model: n_layers packed blocks (weights drawn on the GPU,
+    one seed per layer), one INT4 cache with every layer's history, embedding,
+    final gain and bf16 LM head; a step is one futr_decode_step call."""
+
+    def __init__(self, wl, device: int):
+        import torch
+        from int4_weight_kv_w4a16_gb300 import build, futr
+        build.build()
+        self.torch, self.futr = torch, futr
+        torch.cuda.set_device(device)
+        self.wl, self.shape, self.b, self.vocab = wl, wl.shape, wl.batch, wl.vocab
+        self.cs = futr.make_shape(self.shape)
+        self.lengths = inputs.context_lengths(wl)
+        self.cap = int(max(self.lengths)) + 16
+        nbytes = futr.futr_weights_size(self.cs)
+        self.blobs = []
+        for l in range(wl.n_layers):
+            w = inputs.block_weights_device(self.shape, l)
+            blob = futr.alloc_bytes(nbytes)
+            futr.futr_pack_weights(self.cs, w["wq"], w["wk"], w["wv"], w["wo"], w["wgate"], w["wup"], w["wdown"],
+                                   w["g_attn"], w["g_mlp"], blob)
+            del w
+            self.blobs.append(blob)
+        self.kv = futr.futr_kv_init(self.cs, wl.n_layers, self.b, self.cap,
+                                    futr.alloc_bytes(futr.futr_kv_size(self.cs, wl.n_layers, self.b, self.cap)))
+        self.ws = futr.futr_workspace_init(self.cs, self.b, self.cap,
+                                           futr.alloc_bytes(futr.futr_workspace_size(self.cs, self.b, self.cap)))
+        zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for l in range(wl.n_layers):
+            for s in range(self.b):
+                k, v = inputs.kv_history_device(self.shape, int(self.lengths[s]), seed=1000 * l + s)
+                futr.futr_kv_append(self.kv, l, s, 1, zero, int(self.lengths[s]), k, v)
+        g = torch.Generator(device="cuda").manual_seed(12345)
+        self.embedding = torch.randn((self.vocab, self.shape.hidden), generator=g, device="cuda").to(torch.bfloat16)
+        self.lm_head = (torch.randn((self.vocab, self.shape.hidden), generator=g, device="cuda") * 0.02).to(
+            torch.bfloat16)
+        self.g_final = torch.rand(self.shape.hidden, generator=g, device="cuda") + 0.5
+        self.tokens = torch.from_numpy((np.arange(self.b) * 7919 + 11) % self.vocab).int().cuda()
+        self.pos = torch.from_numpy(np.asarray(self.lengths, np.int32)).cuda()
+        self.logits = torch.empty((self.b, self.vocab), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        st = futr.futr_check(self.ws, self.kv)
+        if st != 0:
+            raise RuntimeError(futr.futr_status_string(st))
+        blk = stage_bytes(self.shape, self.lengths)
+        H = self.shape.hidden
+        self.bytes = {"blocks": wl.n_layers * sum(blk.values()), "embedding": self.b * H * 2,
+                      "lm_head": self.vocab * H * 2 + self.b * H * 2 + self.b * self.vocab * 4}
+
+    def step(self, tokens=None, pos=None, logits=None):
+        self.futr.futr_decode_step(self.tokens if tokens is None else tokens, self.embedding, self.vocab, self.blobs,
+                                   self.kv, self.b, self.pos if pos is None else pos, self.g_final, self.lm_head,
+                                   self.logits if logits is None else logits, self.ws)
+
+    def timed(self, steps: int, warmup: int):
+        torch = self.torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+                for _ in range(steps):
+                    self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        g.replay()
+        torch.cuda.synchronize()
+        st = self.futr.futr_check(self.ws, self.kv)
+        if st != 0:
+            raise RuntimeError(self.futr.futr_status_string(st))
+        return g
+
+    def e2e(self, n: int):
+        """Tokens and positions from pinned host memory, logits back to the host,
+        every step (wall clock)."""
+        torch = self.torch
+        th = self.tokens.cpu().pin_memory()
+        ph = self.pos.cpu().pin_memory()
+        lh = torch.empty((self.b, self.vocab), dtype=torch.float32).pin_memory()
+        td, pd = torch.empty_like(self.tokens), torch.empty_like(self.pos)
+        for k in range(n + 3):
+            if k == 3:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            td.copy_(th, non_blocking=True)
+            pd.copy_(ph, non_blocking=True)
+            self.step(td, pd)
+            lh.copy_(self.logits, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        dt = time.perf_counter() - t0
+        return {"value": 1e6 * dt / n, "unit": STEP_UNIT, "h2d_bytes_per_step": int(8 * self.b),
+                "d2h_bytes_per_step": int(4 * self.b * self.vocab)}
+
+
+def step_oracle_baseline(wl, budget_rows: int = 8192):
+    """The oracle on the host cores, extrapolated: one block-step of this shape
+    and batch (weights pre-dequantized) times n_layers, plus the final norm and
+    LM head on ``budget_rows`` vocabulary rows scaled to the full vocabulary."""
+    import oracle
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sh = wl.shape
+    lengths = inputs.context_lengths(wl)
+    w = inputs.block_weights(sh, 0)
+    wdq = oracle.dequant_block(oracle.pack_block(w))
+    del w
+    x = inputs.activations(sh, wl.batch, 0)
+    cache = oracle.build_cache(inputs.kv_history(sh, lengths, n_outlier=wl.n_outlier, seed=0), sh)
+    pos = np.asarray(lengths)
+    oracle.decode_block(x, wdq, cache, pos, sh)
+    t0 = time.perf_counter()
+    out = oracle.decode_block(x, wdq, cache, pos, sh)
+    t_block = time.perf_counter() - t0
+    r = np.random.default_rng(0)
+    w_rows = inputs.to_bf16_bits(r.standard_normal((budget_rows, sh.hidden)).astype(np.float32) * 0.02)
+    g = r.uniform(0.5, 1.5, sh.hidden).astype(np.float32)
+    t0 = time.perf_counter()
+    oracle.final_logits(out["y"], g, w_rows, sh.rms_eps)
+    t_head = (time.perf_counter() - t0) * wl.vocab / budget_rows
+    us = 1e6 * (t_block * wl.n_layers + t_head)
+    return {"value": round(us, 1), "unit": STEP_UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"1 block-step of {sh.hidden}-hidden batch {wl.batch} x {wl.n_layers} layers + final norm and "
+                      f"LM head on {budget_rows} of {wl.vocab} rows scaled to the vocabulary (float64 numpy)"}
+
+
+def run_step(args, wl):
+    rank, world, local = dist_env()
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    B = StepBench(wl, local)
+    g = B.timed(args.steps, args.warmup)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    st = B.futr.futr_check(B.ws, B.kv)
+    if st != 0:
+        raise RuntimeError(B.futr.futr_status_string(st))
+    us_step = 1000.0 * ms / args.steps
+    value = whole_job_us_per_step(ms, args.steps, world)
+    pk = peaks()
+    total = sum(B.bytes.values())
+    gbs = total / (us_step * 1e-6) / 1e9
+    e2e = B.e2e(min(args.steps, 20))
+    line = {
+        "metric": STEP_METRIC, "value": round(value, 3), "unit": STEP_UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "layers": wl.n_layers, "vocab": wl.vocab, "batch": B.b, "ctx": int(wl.ctx),
+                   "weights": "int4 group-128 fp16 scales; bf16 embedding and LM head",
+                   "l2": f"{sum(B.bytes.values()) / 1e9:.2f} GB streamed per step > L2",
+                   "timing": "CUDA graph of K steps, 164 kernels/step, programmatic dependent launch",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": "whole step", "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
+                     "algorithmic_bytes": int(total), "peak_source": pk["source"]},
+        "tokens_per_s": round(B.b / (us_step * 1e-6), 1),
+        "e2e": e2e, "clocks": clk, "gpu_launches": (2 + 5 * wl.n_layers + 2) * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = step_oracle_baseline(wl)
+    if rank == 0:
+        out = json.dumps(line)
+        print(out, flush=True)
+        if args.out:
+            with open(args.out, "a") as f:
+                f.write(out + "\n")
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -412,6 +605,21 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = inputs.WORKLOADS[args.workload]
+    if wl.vocab > 0:  # the complete model step
+        if args.impl == "reference":
+            rank, world, _ = dist_env()
+            if rank == 0:
+                base = step_oracle_baseline(wl)
+                print(json.dumps({"impl": "reference", "metric": STEP_METRIC, "value": base["value"],
+                                  "unit": STEP_UNIT, "n_gpus": world, "steps": 1, "warmup": 1,
+                                  "ms_per_step": round(base["value"] / 1000, 3), "higher_is_better": False,
+                                  "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                                  "config": {"workload": wl.name, "batch": wl.batch}, "cpu_baseline": base,
+                                  "e2e": {"value": base["value"], "unit": STEP_UNIT, "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0}}), flush=True)
+        else:
+            run_step(args, wl)
+        return
     if args.impl == "reference":
         if args.steps > 20:
             args.steps = 20  # bounded CPU sample

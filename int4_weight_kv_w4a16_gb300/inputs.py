@@ -63,6 +63,7 @@ class Workload:
     n_outlier: int = 4              # outlier key channels per kv-head (x20)
     outlier_gain: float = 20.0
     n_layers: int = 1
+    vocab: int = 0                  # > 0: the full decode step (embedding, n_layers blocks, LM head)
 
 
 TOY = BlockShape(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, inter=768, had_block=64)
@@ -78,6 +79,11 @@ WORKLOADS: Dict[str, Workload] = {
     "llama70b_b1_ctx2048": Workload("llama70b_b1_ctx2048", LLAMA70B, 1, 2048),
     "llama70b_b8_ctx2048": Workload("llama70b_b8_ctx2048", LLAMA70B, 8, 2048),
     "llama70b_b32_ctx2048": Workload("llama70b_b32_ctx2048", LLAMA70B, 32, 2048),
+    # complete 8B model step: 32 blocks + embedding + final norm + bf16 LM head
+    "llama8b_x32_b1_ctx2048": Workload("llama8b_x32_b1_ctx2048", LLAMA8B, 1, 2048, n_layers=32, vocab=128256),
+    "llama8b_x32_b16_ctx2048": Workload("llama8b_x32_b16_ctx2048", LLAMA8B, 16, 2048, n_layers=32, vocab=128256),
+    # two layers + the full head: a few GB on the device, for kernel profiles
+    "llama8b_x2_b1_ctx2048": Workload("llama8b_x2_b1_ctx2048", LLAMA8B, 1, 2048, n_layers=2, vocab=128256),
 }
 
 
@@ -157,3 +163,31 @@ def kv_history(shape: BlockShape, lengths: Sequence[int], n_outlier: int = 4,
             k[h][:, chans[h]] *= np.float32(gain)
         out.append((to_bf16_bits(k), to_bf16_bits(v)))
     return out
+
+
+# Device-side generators for the complete-model workloads (32 layers of fp32
+# weights would not fit a host array comfortably): torch's counter-based
+# generator on the GPU, one seed per layer and component.
+
+def block_weights_device(shape: BlockShape, seed: int, std: float = 0.02):
+    """As ``block_weights``, generated on cuda:0 (dict of fp32 tensors)."""
+    import torch
+    H, I = shape.hidden, shape.inter
+    g = torch.Generator(device="cuda").manual_seed(1_000_003 * (seed + 1))
+    n = lambda *sz: torch.randn(sz, generator=g, device="cuda", dtype=torch.float32) * std
+    return {"wq": n(shape.q_rows, H), "wk": n(shape.kv_rows, H), "wv": n(shape.kv_rows, H),
+            "wo": n(H, shape.q_rows), "wgate": n(I, H), "wup": n(I, H), "wdown": n(H, I),
+            "g_attn": torch.rand(H, generator=g, device="cuda") + 0.5,
+            "g_mlp": torch.rand(H, generator=g, device="cuda") + 0.5}
+
+
+def kv_history_device(shape: BlockShape, length: int, seed: int, n_outlier: int = 4, gain: float = 20.0):
+    """One sequence's cached K, V on cuda:0 (bf16 bits [Hkv, length, d] as int16
+    tensors), N(0, 1) with ``n_outlier`` key channels per kv-head times ``gain``."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(7_000_003 * (seed + 1))
+    k = torch.randn((shape.n_kv_heads, length, shape.head_dim), generator=g, device="cuda")
+    v = torch.randn((shape.n_kv_heads, length, shape.head_dim), generator=g, device="cuda")
+    chans = torch.from_numpy(outlier_channels(shape, n_outlier, seed)).cuda()
+    k.scatter_(2, chans[:, None, :].expand(-1, length, -1), k.gather(2, chans[:, None, :].expand(-1, length, -1)) * gain)
+    return k.to(torch.bfloat16).view(torch.int16), v.to(torch.bfloat16).view(torch.int16)
