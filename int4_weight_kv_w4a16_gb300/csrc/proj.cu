@@ -47,24 +47,33 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
 }
 
-// Position and RoPE (cos, sin) of one head task, loaded ahead of the split
-// handshake where possible: cs[j] pairs dims lane + 32 j and lane + 32 j + d/2.
+// Position and RoPE (cos, sin) of one head task: cs[j] pairs dims lane + 32 j
+// and lane + 32 j + d/2.
 struct HeadPre {
   int p;
   float2 cs[2];
 };
 
-__device__ __forceinline__ HeadPre load_head_pre(const ProjArgs& a, int n, int hg) {
-  HeadPre h;
-  h.p = a.pos[n];
-  h.cs[0] = h.cs[1] = make_float2(1.f, 0.f);
-  if (hg < a.Hq + a.Hkv) {  // q and k heads are rotated by position
-    const int lane = threadIdx.x & 31, half = a.d / 2;
-    const int pp = h.p >= 0 && h.p < a.kv.cap ? h.p : 0;
-    h.cs[0] = a.rope[(size_t)pp * half + lane];
-    if (half > 32) h.cs[1] = a.rope[(size_t)pp * half + lane + 32];
+// The head tasks' positions and RoPE factors in shared memory, loaded by many
+// threads at once ahead of the epilogue: hcs[(task * 2 + j) * 32 + lane],
+// hpos[task].  Item i = (task, lane) for i = first, first + stride, ...
+__device__ __forceinline__ void fill_head_cache(const ProjArgs& a, int rb, float2* hcs, int* hpos, int first,
+                                                int stride) {
+  const int hpr = kRowsPerBlock / a.d, ntask = a.batch * hpr, half = a.d / 2;
+  for (int i = first; i < ntask * 32; i += stride) {
+    const int task = i >> 5, l = i & 31;
+    const int n = task / hpr, hg = rb * hpr + task % hpr;
+    const int p = a.pos[n];
+    float2 c0 = make_float2(1.f, 0.f), c1 = c0;
+    if (hg < a.Hq + a.Hkv) {  // q and k heads are rotated by position
+      const int pp = p >= 0 && p < a.kv.cap ? p : 0;
+      c0 = a.rope[(size_t)pp * half + l];
+      if (half > 32) c1 = a.rope[(size_t)pp * half + l + 32];
+    }
+    hcs[(task * 2) * 32 + l] = c0;
+    hcs[(task * 2 + 1) * 32 + l] = c1;
+    if (l == 0) hpos[task] = p;
   }
-  return h;
 }
 
 template <int J>
@@ -295,21 +304,24 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
       if ((tid & 15) == 0 && n < a.batch) ss[n] = ssq[p];
     }
   }
-  // the residual rows of this block (RESID), the position and RoPE factors of
-  // this warp's first head task (QKV), loaded now so that their latency
-  // overlaps the split handshake
-  HeadPre pre0{};
-  if (EPI == kEpiQkv) {
-    const int hpr = kRowsPerBlock / a.d;
-    if (warp < a.batch * hpr) pre0 = load_head_pre(a, warp / hpr, rb * hpr + warp % hpr);
-  }
+  // the residual rows of this block (RESID): with one batch tile loaded now,
+  // overlapping the split handshake; with more, in one burst after the
+  // reduction, which keeps them out of its registers
+  constexpr bool kEarly = NT == 1;
   __nv_bfloat16 rres[EPI == kEpiResid ? NT * 8 : 1];
-  if (EPI == kEpiResid) {
+  auto load_resid = [&]() {
+    if (EPI == kEpiResid) {
 #pragma unroll
-    for (int n = 0; n < NT * 8; ++n)
-      rres[n] = n < a.batch ? a.resid[(size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid]
-                            : __float2bfloat16_rn(0.f);
-  }
+      for (int n = 0; n < NT * 8; ++n)
+        rres[n] = n < a.batch ? a.resid[(size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid]
+                              : __float2bfloat16_rn(0.f);
+    }
+  };
+  if (kEarly) load_resid();
+  // QKV: the head tasks' positions and RoPE factors go to shared memory after
+  // the epilogue tile and the split-sum groups (the ring is free by then)
+  float2* hcs = reinterpret_cast<float2*>(red + NT * 8 * kRedLd + 4 * kCW * 32);
+  int* hpos = reinterpret_cast<int*>(hcs + a.batch * (kRowsPerBlock / a.d) * 64);
   if (!ok) {
     set_err(a.err, FUTR_ERR_TIMEOUT);
     flag[1] = 1;
@@ -347,7 +359,10 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
       reinterpret_cast<float4*>(rec + n * kRecLd)[c4] = v;
     }
     consumer_sync();
-    if (tid == 0) flag[0] = atom_add_acq_rel_gpu(&a.cnt[rb], 1u) == (unsigned)(a.S - 1) ? 1 : 0;
+    if (tid == 0)
+      flag[0] = atom_add_acq_rel_gpu(&a.cnt[rb], 1u) == (unsigned)(a.S - 1) ? 1 : 0;
+    else if (EPI == kEpiQkv)
+      fill_head_cache(a, rb, hcs, hpos, tid - 1, kCW * 32 - 1);  // overlaps the arrival
     consumer_sync();
     if (!flag[0]) return;
     // The last CTA adds the S records.  With few columns (small batch), G
@@ -357,7 +372,43 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
     const int G = items >= kCW * 32 ? 1 : (kCW * 32) / items;
     float4* gsum = reinterpret_cast<float4*>(red + NT * 8 * kRedLd);  // [G][items], G > 1 only
     const float* part_rb = a.part + (size_t)rb * a.S * a.rec_floats;
-    for (int t = tid; t < G * items; t += kCW * 32) {
+    if (G == 1) {
+      // Many columns (batch >= 4): thread t owns columns t + 128 j and adds
+      // them split by split, the loads of all its columns for one split in
+      // flight together (the sum of each column stays in split order).
+      constexpr int kJ = (NT * 8 * kRecCols + kCW * 32 - 1) / (kCW * 32);
+      float4 s4[kJ];
+      int col[kJ];
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        s4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int e = tid + kCW * 32 * j;
+        col[j] = e < items ? e : -1;  // float4 index n * kRecCols + c4 of the record
+      }
+      const float4* rec4 = reinterpret_cast<const float4*>(part_rb);
+      const size_t step = a.rec_floats / 4;
+      for (int s0 = 0; s0 < a.S; ++s0) {
+        float4 v[kJ];
+#pragma unroll
+        for (int j = 0; j < kJ; ++j)
+          if (col[j] >= 0) v[j] = __ldcg(rec4 + (size_t)s0 * step + col[j]);
+#pragma unroll
+        for (int j = 0; j < kJ; ++j)
+          if (col[j] >= 0) {
+            s4[j].x += v[j].x; s4[j].y += v[j].y; s4[j].z += v[j].z; s4[j].w += v[j].w;
+          }
+      }
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        if (col[j] >= 0) {
+          const int n = col[j] / kRecCols, c4 = col[j] - kRecCols * n;
+          if (c4 < 32)
+            reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4[j];
+          else
+            ss[n] = s4[j].x;
+        }
+    }
+    for (int t = tid; G > 1 && t < G * items; t += kCW * 32) {
       const int grp = t / items, e = t - grp * items;
       const int n = e / kRecCols, c4 = e - kRecCols * n;
       const int s_lo = grp * a.S / G, s_hi = (grp + 1) * a.S / G;
@@ -374,13 +425,7 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
             s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
           }
       }
-      if (G > 1) {
-        gsum[t] = s4;
-      } else if (c4 < 32) {
-        reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4;
-      } else {
-        ss[n] = s4.x;
-      }
+      gsum[t] = s4;
     }
     if (G > 1) {
       consumer_sync();
@@ -401,6 +446,11 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
     consumer_sync();
   }
 
+  if (!kEarly) load_resid();
+  if (EPI == kEpiQkv && a.S == 1) {
+    fill_head_cache(a, rb, hcs, hpos, tid, kCW * 32);
+    consumer_sync();
+  }
   if (EPI == kEpiResid) {
     // consumer thread t owns output row t of the block (kCW * 32 == 128)
 #pragma unroll
@@ -426,11 +476,14 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
       const int n = task / hpr, hl = task % hpr;
       const int hg = rb * hpr + hl;
       const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(ss[n], (float)a.K) + a.eps));
-      const HeadPre pre = task == warp ? pre0 : load_head_pre(a, n, hg);
+      HeadPre hp;
+      hp.p = hpos[task];
+      hp.cs[0] = hcs[(task * 2) * 32 + lane];
+      hp.cs[1] = hcs[(task * 2 + 1) * 32 + lane];
       if (a.d == 128)
-        qkv_head_epilogue<4>(a, red, n, hl, hg, rn, pre);
+        qkv_head_epilogue<4>(a, red, n, hl, hg, rn, hp);
       else
-        qkv_head_epilogue<2>(a, red, n, hl, hg, rn, pre);
+        qkv_head_epilogue<2>(a, red, n, hl, hg, rn, hp);
     }
   }
 }
@@ -517,8 +570,9 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   if (ring < 2) ring = 2;
   p.ring = ring;
   int ring_bytes = ring * p.stage_bytes;
-  // the epilogue tile (+ the split-sum groups of small batches) aliases the ring
-  const int red_bytes = p.nt * 8 * kRedLd * 4 + kCW * 32 * 16;
+  // the epilogue tile, the split-sum groups of small batches and (QKV) the
+  // head tasks' RoPE factors alias the ring (up to 2 heads per row block)
+  const int red_bytes = p.nt * 8 * kRedLd * 4 + kCW * 32 * 16 + (epi == kEpiQkv ? batch * 2 * 512 + 256 : 0);
   if (ring_bytes < red_bytes) ring_bytes = red_bytes;
   p.off_misc = (ring_bytes + 127) & ~127;
   p.smem = (size_t)p.off_misc + misc;
