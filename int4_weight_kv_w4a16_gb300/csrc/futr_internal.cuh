@@ -187,26 +187,40 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_r
                : "r"(smem_u32(smem_row)));
 }
 
-// Nibble pair (bits 4i and 16+4i of w, offset-8 codes) -> exact bf16x2 codes:
-// 0x4300 | u is the bf16 value 128 + u; subtracting 136 leaves u - 8.
-__device__ __forceinline__ uint32_t nib_bf16x2(uint32_t w, int i) {
-  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-  uint32_t r;  // 136 = bf16 0x4308; the difference is exact
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
-  return r;
+// The four bf16x2 registers of a word of offset-8 codes: register i holds the
+// nibbles at bits 4i and 16 + 4i.  0x4300 | u is the bf16 value 128 + u, so
+// subtracting 136 (bf16 0x4308) leaves u - 8 exactly.  Written as one PTX
+// sequence (3 shifts, 4 lop3 "(a & b) | c", 4 bf16x2 subtracts): the
+// compiler's own lowering of the C expression issues more integer-pipe work.
+__device__ __forceinline__ void nib4_bf16x2(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n\t.reg .b32 s1, s2, s3, t0, t1, t2, t3;\n\t"
+      "shr.b32 s1, %4, 4;\n\tshr.b32 s2, %4, 8;\n\tshr.b32 s3, %4, 12;\n\t"
+      "lop3.b32 t0, %4, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "lop3.b32 t1, s1, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "lop3.b32 t2, s2, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "lop3.b32 t3, s3, 0x000F000F, 0x43004300, 0xEA;\n\t"
+      "sub.rn.bf16x2 %0, t0, %5;\n\tsub.rn.bf16x2 %1, t1, %5;\n\t"
+      "sub.rn.bf16x2 %2, t2, %5;\n\tsub.rn.bf16x2 %3, t3, %5;\n\t}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w), "r"(0x43084308u));
 }
 
 // All four fp16x2 registers of a word (slots (i, i+4), i = 0..3) with one
 // shift: fp16 keeps 10 mantissa bits, so a nibble at bits 4-7 of a half is
 // exact too: 0x6400 | u << 4 is 1024 + 16u, and (1024 + 16u) / 16 - 72 = u - 8.
 __device__ __forceinline__ void nib4_f16x2(uint32_t w, uint32_t (&r)[4]) {
-  const uint32_t w8 = w >> 8;
-  const uint32_t t0 = (w & 0x000F000Fu) | 0x64006400u, t1 = (w & 0x00F000F0u) | 0x64006400u;
-  const uint32_t t2 = (w8 & 0x000F000Fu) | 0x64006400u, t3 = (w8 & 0x00F000F0u) | 0x64006400u;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[0]) : "r"(t0), "r"(0x64086408u));             // - 1032
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[1]) : "r"(t1), "r"(0x2C002C00u), "r"(0xD480D480u));  // / 16 - 72
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r[2]) : "r"(t2), "r"(0x64086408u));
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r[3]) : "r"(t3), "r"(0x2C002C00u), "r"(0xD480D480u));
+  // one shift, 4 lop3, then 1032 subtracted (fp16 0x6408) or x / 16 - 72
+  // (fp16 0x2C00, 0xD480)
+  asm("{\n\t.reg .b32 s8, t0, t1, t2, t3;\n\t"
+      "shr.b32 s8, %4, 8;\n\t"
+      "lop3.b32 t0, %4, 0x000F000F, 0x64006400, 0xEA;\n\t"
+      "lop3.b32 t1, %4, 0x00F000F0, 0x64006400, 0xEA;\n\t"
+      "lop3.b32 t2, s8, 0x000F000F, 0x64006400, 0xEA;\n\t"
+      "lop3.b32 t3, s8, 0x00F000F0, 0x64006400, 0xEA;\n\t"
+      "sub.rn.f16x2 %0, t0, %5;\n\tfma.rn.f16x2 %1, t1, %6, %7;\n\t"
+      "sub.rn.f16x2 %2, t2, %5;\n\tfma.rn.f16x2 %3, t3, %6, %7;\n\t}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w), "r"(0x64086408u), "r"(0x2C002C00u), "r"(0xD480D480u));
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {

@@ -127,7 +127,7 @@ __device__ __forceinline__ void issue_tile(const ProjArgs& a, uint8_t* stage, in
 }
 
 template <int NT, int EPI>
-__global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
+__device__ __forceinline__ void proj_body(const ProjArgs& a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rb = blockIdx.x / a.S, sk = blockIdx.x - rb * a.S;
@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
 #pragma unroll
         for (int m = 0; m < kMT; ++m) {
           const uint32_t w = words[m][2 * kp + h];
-          const uint32_t af[4] = {nib_bf16x2(w, 0), nib_bf16x2(w, 1), nib_bf16x2(w, 2), nib_bf16x2(w, 3)};
+          uint32_t af[4];
+          nib4_bf16x2(w, af);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(dpart[m][nt], af, bfr[nt][2 * h], bfr[nt][2 * h + 1]);
         }
@@ -489,15 +490,34 @@ __global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
 }
 
 template <int NT, int EPI>
+__global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
+  proj_body<NT, EPI>(a);
+}
+
+// Three or four batch tiles: at most 128 registers, so three CTAs share an SM.
+template <int NT, int EPI>
+__global__ void __maxnreg__(128) proj_kernel_wide(const ProjArgs a) {
+  proj_body<NT, EPI>(a);
+}
+
+template <int NT, int EPI>
+constexpr void (*proj_entry())(ProjArgs) {
+  if constexpr (NT >= 3)
+    return proj_kernel_wide<NT, EPI>;
+  else
+    return proj_kernel<NT, EPI>;
+}
+
+template <int NT, int EPI>
 cudaError_t configure(int dev) {
   static unsigned long long configured = 0;  // one bit per device
   if (configured & (1ull << (dev & 63))) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(proj_entry<NT, EPI>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kProjMaxSmem);
   if (e != cudaSuccess) return e;
   // every kernel of the step asks for the maximum shared-memory carveout, so
   // CTAs of consecutive kernels can share an SM (programmatic overlap)
-  e = cudaFuncSetAttribute(proj_kernel<NT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(proj_entry<NT, EPI>(), cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   configured |= 1ull << (dev & 63);
@@ -521,7 +541,7 @@ cudaError_t launch_one(const ProjArgs& a, int grid, size_t smem, cudaStream_t st
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, proj_kernel<NT, EPI>, a);
+  return cudaLaunchKernelEx(&cfg, proj_entry<NT, EPI>(), a);
 }
 
 template <int EPI>
@@ -542,7 +562,7 @@ int resident_ctas(int nt, int epi, size_t smem) {
   if (nt == NT_ && epi == EPI_) {                                                         \
     e = configure<NT_, EPI_>(dev);                                                        \
     if (e == cudaSuccess)                                                                 \
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_kernel<NT_, EPI_>, kThreads, smem); \
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_entry<NT_, EPI_>(), kThreads, smem); \
   }
   FUTR_OCC(1, 0) FUTR_OCC(2, 0) FUTR_OCC(3, 0) FUTR_OCC(4, 0)
   FUTR_OCC(1, 1) FUTR_OCC(2, 1) FUTR_OCC(3, 1) FUTR_OCC(4, 1)
