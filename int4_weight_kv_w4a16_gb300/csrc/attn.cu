@@ -7,20 +7,26 @@
 // after: the query is rotated the same way (in the QKV epilogue) and the
 // attention output is rotated back here.
 //
-// Grid (NC, kv-head, sequence); the NC CTAs of one (sequence, kv-head) form a
-// thread-block cluster and split the context into NC contiguous ranges of
-// 64-position tiles.  In a CTA:
+// Grid (NC, kv-head x head sub-group, sequence); the NC CTAs of one
+// (sequence, kv-head, sub-group) form a thread-block cluster and split the
+// context into NC contiguous ranges of 64-position tiles.  A kv-head's G query
+// heads go to ceil(G / 8) sub-groups of at most 8 heads (one for Llama's G of
+// 4 and 8).  In a CTA:
 //   warp 4 (producer) streams the range's tiles (key codes, value codes, key
 //     and value scales: four 1-D bulk copies per tile) through a ring of
 //     shared-memory stages with mbarrier completion;
-//   warps 0..3 (consumers) take one 16-position sub-tile of every tile:
-//     S = q' K^T: mma.m16n8k16 f16, A = the G query heads of this kv-head
-//       (rows >= G are zero) as an fp16 pair hi + lo of the fp32 query (two
-//       MMAs), B = key codes converted in registers (exact);
-//     score = S * key_scale * log2(e)/sqrt(d);
+//   warps 0..3 (consumers) take one 16-position sub-tile of every tile and
+//     work in the transposed orientation, positions along the MMA's 16 rows:
+//     S^T = K q'^T: mma.m16n8k16 f16, A = key codes converted in registers
+//       (exact), B = the query heads as columns, each fp32 query as an fp16
+//       pair hi + lo: the hi parts take the first half of the columns, the lo
+//       parts the second half, so one MMA carries both (4 heads per n-tile of
+//       8 columns; 8 heads in two n-tiles);
+//     score = (hi + lo column sum) * key_scale * log2(e)/sqrt(d);
 //     online softmax in fp32 (running max m, normalizer l, output rescale);
-//     O += P V: A = fp16(p * value_scale) as an fp16 pair hi + lo, B = value
-//       codes converted in registers.
+//     O^T += V^T P^T: A = value codes converted in registers, B = fp16(p *
+//       value_scale) as an fp16 pair hi + lo in the same column split (the
+//       score fragment becomes the B operand by an 8x8 register transpose).
 // The 4 warps merge (m, l, O) in shared memory.  Then the cluster synchronises
 // (hardware cluster barrier) and the leader CTA reads the other ranges'
 // (m, l, O) from their shared memory (distributed shared memory), merges them
@@ -41,14 +47,20 @@ constexpr int kTilePos = 16 * kAttnCW;            // positions per ring stage: o
 constexpr int kAttnRing = 4;
 constexpr int kMaxCluster = 16;
 
+constexpr int kMaxSubHeads = 8;  // query heads of one CTA (two n-tiles of hi + lo columns)
+
+// Query heads of one sub-group, and the sub-groups of a kv-head.
+__host__ __device__ inline int attn_nsub(int G) { return (G + kMaxSubHeads - 1) / kMaxSubHeads; }
+__host__ __device__ inline int attn_gc(int G) { return (G + attn_nsub(G) - 1) / attn_nsub(G); }
+
 template <int D>
 struct AttnLayout {
   static constexpr int kCodes = kTilePos * D / 2;            // key (or value) codes of a tile, bytes
   static constexpr int kStage = 2 * kCodes + 4 * kTilePos;   // + key and value scales (fp16)
-  // after the ring: the query A fragments [D/16][hi, lo][32 lanes] (uint4);
+  // after the ring: the query B fragments [D/16][2 n-tiles][32 lanes] (uint2);
   // then floats cm, cl [warps][G]; co [warps][G][D]; mO [G][D]; mm, ml [G];
-  // wm, wl [kMaxCluster][G]
-  static constexpr int kQFrag = (D / 16) * 2 * 32 * 16;
+  // wm, wl [kMaxCluster][G] (G = the heads of one sub-group)
+  static constexpr int kQFrag = (D / 16) * 2 * 32 * 8;
   __host__ __device__ static int floats(int G) { return 2 * kAttnCW * G + kAttnCW * G * D + G * D + 2 * G + 2 * kMaxCluster * G; }
   __host__ __device__ static size_t bytes(int G) {
     return (size_t)kAttnRing * kStage + kQFrag + 4 * (size_t)floats(G) + 2 * kAttnRing * 8;
@@ -80,17 +92,22 @@ __device__ __forceinline__ float4 ld_dsmem4(const float4* local, uint32_t rank) 
   return v;
 }
 
-template <int D>
+// NTQ: n-tiles of query columns (1: at most 4 heads, 2: at most 8).
+template <int D, int NTQ>
 __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a) {
   constexpr int J = D / 32;
   using Lay = AttnLayout<D>;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int sp = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, NC = gridDim.x;
+  const int nsub = attn_nsub(a.G);
+  const int sp = blockIdx.x, kvh = blockIdx.y / nsub, sub = blockIdx.y - kvh * nsub, b = blockIdx.z, NC = gridDim.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int G = a.G, cap = a.kv.cap;
+  const int cap = a.kv.cap;
+  // G: heads per sub-group (the shared-memory layout); Gv: this sub-group's
+  // heads, query heads hq0 .. hq0 + Gv - 1
+  const int G = attn_gc(a.G), hq0 = kvh * a.G + sub * G, Gv = min(G, a.G - sub * G);
 
   uint8_t* stages = smem;
-  uint4* qf = reinterpret_cast<uint4*>(smem + kAttnRing * Lay::kStage);  // [D/16][2][32]
+  uint2* qf = reinterpret_cast<uint2*>(smem + kAttnRing * Lay::kStage);  // [D/16][NTQ][32]
   float* cm = reinterpret_cast<float*>(smem + kAttnRing * Lay::kStage + Lay::kQFrag);  // [warps][G]
   float* cl = cm + kAttnCW * G;                                          // [warps][G]
   float* co = cl + kAttnCW * G;                                          // [warps][G][D]
@@ -169,36 +186,41 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
     }
   } else {
     // ----------------------------------------------------------- consumers --
-    // query fragments (A operand of q.k), once per CTA into shared memory:
-    // rows = heads of this group, padded to 16; each fp32 pair becomes an
-    // fp16 hi register and an fp16 lo register (the remainder)
+    // query fragments (B operand of K q'^T), once per CTA into shared memory:
+    // column c of n-tile nt is head slot (8 nt + c) mod 4 NTQ, its hi part
+    // (fp16 of the fp32 query) in the first half of the columns, its lo part
+    // (fp16 of the remainder) in the second; slots >= Gv are zero
     {
-      const float* q = a.qrot + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
-      const float2 zero = make_float2(0.f, 0.f);
-      for (int item = tid; item < (D / 16) * 32; item += kAttnCW * 32) {
-        const int ks = item >> 5, ln = item & 31, gq = ln >> 2, tq = ln & 3;
-        const int c = 16 * ks + 2 * tq;
-        const float2 f0 = gq < G ? *reinterpret_cast<const float2*>(q + gq * D + c) : zero;
-        const float2 f1 = gq + 8 < G ? *reinterpret_cast<const float2*>(q + (gq + 8) * D + c) : zero;
-        const float2 f2 = gq < G ? *reinterpret_cast<const float2*>(q + gq * D + c + 8) : zero;
-        const float2 f3 = gq + 8 < G ? *reinterpret_cast<const float2*>(q + (gq + 8) * D + c + 8) : zero;
-        uint4 hi, lo;
-        split_half2(f0.x, f0.y, hi.x, lo.x);
-        split_half2(f1.x, f1.y, hi.y, lo.y);
-        split_half2(f2.x, f2.y, hi.z, lo.z);
-        split_half2(f3.x, f3.y, hi.w, lo.w);
-        qf[(2 * ks) * 32 + ln] = hi;
-        qf[(2 * ks + 1) * 32 + ln] = lo;
+      const float* q = a.qrot + ((size_t)b * a.Hq + hq0) * D;
+      for (int item = tid; item < (D / 16) * NTQ * 32; item += kAttnCW * 32) {
+        const int ln = item & 31, ks = (item >> 5) / NTQ, nt = (item >> 5) - NTQ * ks;
+        const int col = 8 * nt + (ln >> 2), part = col / (4 * NTQ), hs = col - part * 4 * NTQ;
+        const int k0 = 16 * ks + 2 * (ln & 3);
+        uint2 v = make_uint2(0u, 0u);
+        if (hs < Gv) {
+          const float2 f0 = *reinterpret_cast<const float2*>(q + hs * D + k0);
+          const float2 f1 = *reinterpret_cast<const float2*>(q + hs * D + k0 + 8);
+          uint32_t h0, l0q, h1, l1q;
+          split_half2(f0.x, f0.y, h0, l0q);
+          split_half2(f1.x, f1.y, h1, l1q);
+          v = part ? make_uint2(l0q, l1q) : make_uint2(h0, h1);
+        }
+        qf[(ks * NTQ + nt) * 32 + ln] = v;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kAttnCW * 32) : "memory");  // consumers only
     }
 
+    // This lane's two head slots (columns 2t, 2t + 1 of each n-tile, hi and
+    // lo columns of one head carry the same slot): running max m, normalizer
+    // l (a partial sum over this lane's positions until the end)
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[D / 8][4];
+    float o[D / 16][NTQ][4];  // O^T: rows = dims 16 j + g (+ 8), columns 2t, 2t + 1
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
+    for (int j = 0; j < D / 16; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) o[nd][e] = 0.f;
+      for (int nt = 0; nt < NTQ; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[j][nt][e] = 0.f;
 
     const unsigned long long deadline = global_ns() + kWaitNs;
     int slot = 0;
@@ -214,99 +236,109 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
       const __half* vsc = ksc + kTilePos;
       const int npos = min(kTilePos, L - (tile0 + i) * kTilePos);
       if (16 * warp < npos) {
-      // S = q' K^T for the two 8-position halves h; the hi and lo query
-      // parts accumulate separately (four independent MMA chains)
-      float s[2][4], s_lo[2][4];
+        // S^T = K q'^T over the D/16 k-steps; even and odd k-steps in two
+        // accumulators (shorter MMA chains)
+        float sa[NTQ][4], sb[NTQ][4];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int nt = 0; nt < NTQ; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s[h][e] = s_lo[h][e] = 0.f;
-      const uint32_t* kw0 = reinterpret_cast<const uint32_t*>(Ks + (size_t)(2 * warp) * (4 * D) + lane * (D / 8));
-      const uint32_t* kw1 = reinterpret_cast<const uint32_t*>(Ks + (size_t)(2 * warp + 1) * (4 * D) + lane * (D / 8));
+          for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+        const uint32_t* kw0 = reinterpret_cast<const uint32_t*>(Ks + (size_t)(2 * warp) * (4 * D) + lane * (D / 8));
+        const uint32_t* kw1 = reinterpret_cast<const uint32_t*>(Ks + (size_t)(2 * warp + 1) * (4 * D) + lane * (D / 8));
 #pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        const uint4 h0 = qf[(4 * j) * 32 + lane], l0q = qf[(4 * j + 1) * 32 + lane];
-        const uint4 h1 = qf[(4 * j + 2) * 32 + lane], l1q = qf[(4 * j + 3) * 32 + lane];
-        const uint32_t qa0[4] = {h0.x, h0.y, h0.z, h0.w}, ql0[4] = {l0q.x, l0q.y, l0q.z, l0q.w};
-        const uint32_t qa1[4] = {h1.x, h1.y, h1.z, h1.w}, ql1[4] = {l1q.x, l1q.y, l1q.z, l1q.w};
+        for (int j = 0; j < D / 32; ++j) {
+          // a code word holds the key's B-operand pairs of k-steps 2j and 2j+1;
+          // the two 8-position halves stack into the A operand's 16 rows
+          uint32_t c0[4], c1[4];
+          nib4_f16x2(kw0[j], c0);
+          nib4_f16x2(kw1[j], c1);
+          const uint32_t ae[4] = {c0[0], c1[0], c0[1], c1[1]};
+          const uint32_t ao[4] = {c0[2], c1[2], c0[3], c1[3]};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t kk[4];
-          nib4_f16x2(h == 0 ? kw0[j] : kw1[j], kk);
-          const uint32_t k0 = kk[0], k1 = kk[1], k2 = kk[2], k3 = kk[3];
-          mma_f16_16816(s[h], qa0, k0, k1);
-          mma_f16_16816(s[h], qa1, k2, k3);
-          mma_f16_16816(s_lo[h], ql0, k0, k1);
-          mma_f16_16816(s_lo[h], ql1, k2, k3);
+          for (int nt = 0; nt < NTQ; ++nt) {
+            const uint2 qe = qf[((2 * j) * NTQ + nt) * 32 + lane];
+            const uint2 qo = qf[((2 * j + 1) * NTQ + nt) * 32 + lane];
+            mma_f16_16816(sa[nt], ae, qe.x, qe.y);
+            mma_f16_16816(sb[nt], ao, qo.x, qo.y);
+          }
         }
-      }
+        // hi + lo: with one n-tile the lo column of this lane's heads sits in
+        // lane t ^ 2; with two, in the second n-tile.  Both lanes of a pair
+        // end with the same sums (addition commutes).
+        float sv[4];  // [key half][head]: (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[h][e] += s_lo[h][e];
-      float sc[2][4], vsv[2][2];
-      bool valid[2][2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int pl = 16 * warp + 8 * h + 2 * t + e;
-          valid[h][e] = pl < npos;
-          const float kscale = valid[h][e] ? __half2float(ksc[pl]) * a.qk_scale_log2 : 0.f;
-          vsv[h][e] = valid[h][e] ? __half2float(vsc[pl]) : 0.f;
-          sc[h][e] = valid[h][e] ? s[h][e] * kscale : -INFINITY;
-          sc[h][2 + e] = valid[h][e] ? s[h][2 + e] * kscale : -INFINITY;
+        for (int e = 0; e < 4; ++e) {
+          if (NTQ == 1) {
+            const float v = sa[0][e] + sb[0][e];
+            sv[e] = v + __shfl_xor_sync(0xffffffffu, v, 2);
+          } else {
+            sv[e] = (sa[0][e] + sb[0][e]) + (sa[1][e] + sb[1][e]);
+          }
         }
-      float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-      float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float corr0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-      const float corr1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-      float pr[2][4];
+        const int pk0 = 16 * warp + g, pk1 = pk0 + 8;
+        const bool v0 = pk0 < npos, v1 = pk1 < npos;
+        const float ks0 = v0 ? __half2float(ksc[pk0]) * a.qk_scale_log2 : 0.f;
+        const float ks1 = v1 ? __half2float(ksc[pk1]) * a.qk_scale_log2 : 0.f;
+        const float vs0 = v0 ? __half2float(vsc[pk0]) : 0.f;
+        const float vs1 = v1 ? __half2float(vsc[pk1]) : 0.f;
+        const float sc0 = v0 ? sv[0] * ks0 : -INFINITY, sc1 = v0 ? sv[1] * ks0 : -INFINITY;
+        const float sc2 = v1 ? sv[2] * ks1 : -INFINITY, sc3 = v1 ? sv[3] * ks1 : -INFINITY;
+        // tile max of each head over the 16 positions (lanes g = 0..7)
+        float mx0 = fmaxf(sc0, sc2), mx1 = fmaxf(sc1, sc3);
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          pr[h][e] = valid[h][e] ? exp2f(sc[h][e] - mn0) : 0.f;
-          pr[h][2 + e] = valid[h][e] ? exp2f(sc[h][2 + e] - mn1) : 0.f;
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
         }
-      l0 = l0 * corr0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-      l1 = l1 * corr1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-      m0 = mn0;
-      m1 = mn1;
-      // rescale O only when some row's running max moved (corr = 1 otherwise:
-      // the product would leave O unchanged)
-      if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float corr0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+        const float corr1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+        const float p0 = v0 ? exp2f(sc0 - mn0) : 0.f, p1 = v0 ? exp2f(sc1 - mn1) : 0.f;
+        const float p2 = v1 ? exp2f(sc2 - mn0) : 0.f, p3 = v1 ? exp2f(sc3 - mn1) : 0.f;
+        l0 = l0 * corr0 + (p0 + p2);
+        l1 = l1 * corr1 + (p1 + p3);
+        m0 = mn0;
+        m1 = mn1;
+        // rescale O only when some head's running max moved (corr = 1
+        // otherwise: the product would leave O unchanged)
+        if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
 #pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          o[nd][0] *= corr0;
-          o[nd][1] *= corr0;
-          o[nd][2] *= corr1;
-          o[nd][3] *= corr1;
+          for (int j = 0; j < D / 16; ++j)
+#pragma unroll
+            for (int nt = 0; nt < NTQ; ++nt) {
+              o[j][nt][0] *= corr0;
+              o[j][nt][1] *= corr1;
+              o[j][nt][2] *= corr0;
+              o[j][nt][3] *= corr1;
+            }
         }
-      }
-      // P operand = p * value_scale as an fp16 pair hi + lo (hi = fp16(v),
-      // lo = fp16(v - hi)): two MMAs keep ~22 bits of each weight.
-      uint32_t pa[4], pl[4];
-      split_half2(pr[0][0] * vsv[0][0], pr[0][1] * vsv[0][1], pa[0], pl[0]);
-      split_half2(pr[0][2] * vsv[0][0], pr[0][3] * vsv[0][1], pa[1], pl[1]);
-      split_half2(pr[1][0] * vsv[1][0], pr[1][1] * vsv[1][1], pa[2], pl[2]);
-      split_half2(pr[1][2] * vsv[1][0], pr[1][3] * vsv[1][1], pa[3], pl[3]);
-      const uint32_t* vw = reinterpret_cast<const uint32_t*>(Vs + (size_t)warp * (8 * D) + lane * (D / 4));
+        // P^T operand: p * value_scale as an fp16 pair hi + lo (hi = fp16(v),
+        // lo = fp16(v - hi)), hi in the first half of the columns; the
+        // (position, column) fragment is transposed to (column, position)
+        uint32_t ht, lt, hb, lb;
+        split_half2(p0 * vs0, p1 * vs0, ht, lt);
+        split_half2(p2 * vs1, p3 * vs1, hb, lb);
+        uint32_t bt[NTQ], bb[NTQ];
+        if (NTQ == 1) {
+          bt[0] = movmatrix_trans(t >= 2 ? lt : ht);
+          bb[0] = movmatrix_trans(t >= 2 ? lb : hb);
+        } else {
+          bt[0] = movmatrix_trans(ht);
+          bb[0] = movmatrix_trans(hb);
+          bt[NTQ - 1] = movmatrix_trans(lt);
+          bb[NTQ - 1] = movmatrix_trans(lb);
+        }
+        const uint32_t* vw = reinterpret_cast<const uint32_t*>(Vs + (size_t)warp * (8 * D) + lane * (D / 4));
 #pragma unroll
-      for (int j = 0; j < D / 16; ++j) {
-        uint32_t vv[4];
-        nib4_f16x2(vw[j], vv);
-        const uint32_t v0 = vv[0], v1 = vv[1], v2 = vv[2], v3 = vv[3];
-        mma_f16_16816(o[2 * j], pa, v0, v1);
-        mma_f16_16816(o[2 * j + 1], pa, v2, v3);
-        mma_f16_16816(o[2 * j], pl, v0, v1);
-        mma_f16_16816(o[2 * j + 1], pl, v2, v3);
-      }
+        for (int j = 0; j < D / 16; ++j) {
+          // a value code word holds the B-operand pairs of dims 16j + g and
+          // 16j + 8 + g: as the A operand of V^T they are rows g and g + 8
+          uint32_t vv[4];
+          nib4_f16x2(vw[j], vv);
+          const uint32_t av[4] = {vv[0], vv[2], vv[1], vv[3]};
+#pragma unroll
+          for (int nt = 0; nt < NTQ; ++nt) mma_f16_16816(o[j][nt], av, bt[nt], bb[nt]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage
@@ -315,32 +347,40 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
         phase ^= 1u;
       }
     }
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-    // this warp's (m, l, O) rows to shared memory
-    if (g < G) {
-      if (t == 0) {
-        cm[warp * G + g] = m0;
-        cl[warp * G + g] = l0;
-      }
 #pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        co[(warp * G + g) * D + 8 * nd + 2 * t] = o[nd][0];
-        co[(warp * G + g) * D + 8 * nd + 2 * t + 1] = o[nd][1];
-      }
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
     }
-    if (g + 8 < G) {
-      if (t == 0) {
-        cm[warp * G + g + 8] = m1;
-        cl[warp * G + g + 8] = l1;
-      }
+    // hi + lo columns of O^T
 #pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        co[(warp * G + g + 8) * D + 8 * nd + 2 * t] = o[nd][2];
-        co[(warp * G + g + 8) * D + 8 * nd + 2 * t + 1] = o[nd][3];
+    for (int j = 0; j < D / 16; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (NTQ == 1)
+          o[j][0][e] += __shfl_xor_sync(0xffffffffu, o[j][0][e], 2);
+        else
+          o[j][0][e] += o[j][NTQ - 1][e];
+      }
+
+    // this warp's (m, l, O) rows to shared memory: the lanes with the hi
+    // columns write their two heads
+    const int ha = NTQ == 1 ? 2 * (t & 1) : 2 * t;
+    if (NTQ > 1 || t < 2) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = ha + e;
+        if (h < Gv) {
+          if (g == 0) {
+            cm[warp * G + h] = e ? m1 : m0;
+            cl[warp * G + h] = e ? l1 : l0;
+          }
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            co[(warp * G + h) * D + 16 * j + g] = o[j][0][e];
+            co[(warp * G + h) * D + 16 * j + 8 + g] = o[j][0][2 + e];
+          }
+        }
       }
     }
   }
@@ -348,7 +388,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
   __syncthreads();
 
   // ---- merge the 4 warps: (mO, mm, ml) of this range
-  for (int e = tid; e < G * D; e += kAttnThreads) {
+  for (int e = tid; e < Gv * D; e += kAttnThreads) {
     const int r = e / D, i = e % D;
     float M = -INFINITY;
     for (int w = 0; w < kAttnCW; ++w) M = fmaxf(M, cm[w * G + r]);
@@ -372,13 +412,14 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
     // ---- the leader merges the NC ranges in range order
     for (int i = tid; i < NC * G; i += kAttnThreads) {
       const int r = i / G, h = i - r * G;
+      if (h >= Gv) continue;
       const float vm = r == 0 ? mm[h] : ld_dsmem(&mm[h], (uint32_t)r);
       const float vl = r == 0 ? ml[h] : ld_dsmem(&ml[h], (uint32_t)r);
       wm[i] = vm;
       wl[i] = vl;
     }
     __syncthreads();
-    if (tid < G) {
+    if (tid < Gv) {
       float M = -INFINITY;
       for (int r = 0; r < NC; ++r) M = fmaxf(M, wm[r * G + tid]);
       float Lr = 0.f;
@@ -391,7 +432,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
     }
     __syncthreads();
     float4* mO4 = reinterpret_cast<float4*>(mO);
-    for (int e4 = tid; e4 < G * D / 4; e4 += kAttnThreads) {
+    for (int e4 = tid; e4 < Gv * D / 4; e4 += kAttnThreads) {
       const int h = (4 * e4) / D;
       // every range's value first (independent remote loads in flight), then
       // the weighted sum in range order
@@ -411,13 +452,13 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
     }
     __syncthreads();
     // ---- normalize, rotate back, store bf16 (an empty context stores zeros)
-    for (int r = warp; r < G; r += kAttnThreads / 32) {
+    for (int r = warp; r < Gv; r += kAttnThreads / 32) {
       const float inv = cm[r] > 0.f ? __fdiv_rn(1.0f, cm[r]) : 0.f;
       float v[J];
 #pragma unroll
       for (int j = 0; j < J; ++j) v[j] = mO[r * D + lane + 32 * j] * inv;
       warp_fwht<J>(v, a.nh, a.had_c);
-      __nv_bfloat16* out = a.out + ((size_t)b * a.Hq + (size_t)kvh * G + r) * D;
+      __nv_bfloat16* out = a.out + ((size_t)b * a.Hq + (size_t)hq0 + r) * D;
 #pragma unroll
       for (int j = 0; j < J; ++j) out[lane + 32 * j] = __float2bfloat16_rn(v[j]);
     }
@@ -426,26 +467,25 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
   if (NC > 1) cluster_sync_all();  // the leader is done reading the other CTAs' shared memory
 }
 
-template <int D>
+template <int D, int NTQ>
 cudaError_t configure_attn(int dev) {
   static unsigned long long configured = 0;  // one bit per device
   if (configured & (1ull << (dev & 63))) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, NTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(attn_kernel<D, NTQ>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(attn_kernel<D, NTQ>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   configured |= 1ull << (dev & 63);
   return cudaSuccess;
 }
 
-template <int D>
-cudaLaunchConfig_t attn_config(const AttnPlan& p, int Hkv, int batch, cudaStream_t st, cudaLaunchAttribute* attr,
+cudaLaunchConfig_t attn_config(const AttnPlan& p, int ny, int batch, cudaStream_t st, cudaLaunchAttribute* attr,
                                bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.NC, (unsigned)Hkv, (unsigned)batch);
+  cfg.gridDim = dim3((unsigned)p.NC, (unsigned)ny, (unsigned)batch);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
@@ -465,58 +505,71 @@ cudaLaunchConfig_t attn_config(const AttnPlan& p, int Hkv, int batch, cudaStream
   return cfg;
 }
 
-template <int D>
+template <int D, int NTQ>
 cudaError_t launch_d(const AttnPlan& p, const AttnArgs& a, cudaStream_t st, bool pdl) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = configure_attn<D>(dev);
+  e = configure_attn<D, NTQ>(dev);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = attn_config<D>(p, a.Hkv, a.batch, st, attr, pdl);
-  return cudaLaunchKernelEx(&cfg, attn_kernel<D>, a);
+  const cudaLaunchConfig_t cfg = attn_config(p, a.Hkv * attn_nsub(a.G), a.batch, st, attr, pdl);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<D, NTQ>, a);
 }
 
 // Largest cluster the device schedules for this kernel (at most kMaxCluster).
-template <int D>
+template <int D, int NTQ>
 int max_cluster(size_t smem) {
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || configure_attn<D>(dev) != cudaSuccess) return 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || configure_attn<D, NTQ>(dev) != cudaSuccess) return 1;
   AttnPlan p{};
   p.NC = 1;
   p.smem = smem;
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = attn_config<D>(p, 1, 1, 0, attr, false);
+  cudaLaunchConfig_t cfg = attn_config(p, 1, 1, 0, attr, false);
   cfg.numAttrs = 0;  // the query wants no cluster dimension set
-  if (cudaOccupancyMaxPotentialClusterSize(&n, attn_kernel<D>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxPotentialClusterSize(&n, attn_kernel<D, NTQ>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     return 1;
   }
   return n < kMaxCluster ? n : kMaxCluster;
 }
 
-template <int D>
+template <int D, int NTQ>
 int resident_attn(size_t smem) {
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || configure_attn<D>(dev) != cudaSuccess) return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D>, kAttnThreads, smem) != cudaSuccess) {
+  if (cudaGetDevice(&dev) != cudaSuccess || configure_attn<D, NTQ>(dev) != cudaSuccess) return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, NTQ>, kAttnThreads, smem) != cudaSuccess) {
     cudaGetLastError();
     return 1;
   }
   return n;
 }
 
+// The four instantiations, by head dim and query n-tiles.
+int max_cluster_any(int D, int ntq, size_t smem) {
+  if (D == 128) return ntq == 1 ? max_cluster<128, 1>(smem) : max_cluster<128, 2>(smem);
+  return ntq == 1 ? max_cluster<64, 1>(smem) : max_cluster<64, 2>(smem);
+}
+
+int resident_attn_any(int D, int ntq, size_t smem) {
+  if (D == 128) return ntq == 1 ? resident_attn<128, 1>(smem) : resident_attn<128, 2>(smem);
+  return ntq == 1 ? resident_attn<64, 1>(smem) : resident_attn<64, 2>(smem);
+}
+
 }  // namespace
 
 AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int force_split) {
   AttnPlan p{};
-  const int G = s.n_q_heads / s.n_kv_heads, D = s.head_dim;
-  p.smem = D == 128 ? AttnLayout<128>::bytes(G) : AttnLayout<64>::bytes(G);
-  const int lim = D == 128 ? max_cluster<128>(p.smem) : max_cluster<64>(p.smem);
-  const int fit = D == 128 ? resident_attn<128>(p.smem) : resident_attn<64>(p.smem);
-  // context ranges per (sequence, kv-head): fewest waves of resident CTAs x
-  // tiles per range (+ the merge), within the cluster limit and the tiles
-  const long long pairs = (long long)batch * s.n_kv_heads, slots = (long long)n_sm * (fit > 0 ? fit : 1);
+  const int G = s.n_q_heads / s.n_kv_heads, D = s.head_dim, gc = attn_gc(G), ntq = gc <= 4 ? 1 : 2;
+  p.smem = D == 128 ? AttnLayout<128>::bytes(gc) : AttnLayout<64>::bytes(gc);
+  const int lim = max_cluster_any(D, ntq, p.smem);
+  const int fit = resident_attn_any(D, ntq, p.smem);
+  // context ranges per (sequence, kv-head, head sub-group): fewest waves of
+  // resident CTAs x tiles per range (+ the merge), within the cluster limit
+  // and the tiles
+  const long long pairs = (long long)batch * s.n_kv_heads * attn_nsub(G);
+  const long long slots = (long long)n_sm * (fit > 0 ? fit : 1);
   const int tiles = (cap + kTilePos - 1) / kTilePos;
   int nc = 1;
   double best = 1e30;
@@ -537,7 +590,9 @@ AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int f
 }
 
 cudaError_t launch_attention(const AttnPlan& p, AttnArgs a, int d, cudaStream_t st, bool pdl) {
-  return d == 128 ? launch_d<128>(p, a, st, pdl) : launch_d<64>(p, a, st, pdl);
+  const bool one = attn_gc(a.G) <= 4;
+  if (d == 128) return one ? launch_d<128, 1>(p, a, st, pdl) : launch_d<128, 2>(p, a, st, pdl);
+  return one ? launch_d<64, 1>(p, a, st, pdl) : launch_d<64, 2>(p, a, st, pdl);
 }
 
 }  // namespace futr

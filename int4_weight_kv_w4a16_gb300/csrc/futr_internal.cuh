@@ -229,6 +229,14 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 // v0, v1 -> fp16x2 hi = (fp16(v0), fp16(v1)) and lo = fp16 of the remainders.
+// Transpose of an 8x8 16-bit matrix held as a warp fragment (thread i:
+// row i / 4, columns 2 (i % 4) and 2 (i % 4) + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
 __device__ __forceinline__ void split_half2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(v0, v1);
   const float2 hf = __half22float2(h);

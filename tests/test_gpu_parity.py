@@ -7,6 +7,8 @@ to the GPU's) and, for the token appended inside the step, the GPU's cache
 entries (that append depends on the fp32 accumulation order of the QKV
 projection; its codes are checked to within one step against the oracle's).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -184,6 +186,22 @@ def test_decode_toy_batch_sweep(batch):
     if batch > 2:
         lengths[1:3] = [15, 16]
     run_case(TOY, batch, list(lengths), seed=batch, chunks=[13, 64, 200] if batch % 2 else None)
+
+
+# Query heads per kv-head from 1 to 16: one n-tile of query columns (up to 4
+# heads), two (up to 8), and two sub-groups of a kv-head (12, 16).
+GROUP_SHAPES = {
+    "g1": dataclasses.replace(TOY, n_q_heads=2, n_kv_heads=2),
+    "g3": dataclasses.replace(TOY, n_q_heads=6, n_kv_heads=2),
+    "g6_d128": dataclasses.replace(TOY, n_q_heads=6, n_kv_heads=1, head_dim=128, had_block=128),
+    "g12": dataclasses.replace(TOY, n_q_heads=12, n_kv_heads=1),
+    "g16": dataclasses.replace(TOY, n_q_heads=16, n_kv_heads=1),
+}
+
+
+@pytest.mark.parametrize("name", list(GROUP_SHAPES))
+def test_decode_query_group_sizes(name):
+    run_case(GROUP_SHAPES[name], 3, [0, 70, 129], seed=11)
 
 
 def test_decode_8b_b1_ctx1024():
