@@ -92,9 +92,17 @@ __device__ __forceinline__ float4 ld_dsmem4(const float4* local, uint32_t rank) 
   return v;
 }
 
+// 2^x by the hardware approximation (relative error ~2^-22; arguments here are
+// <= 0, results below 2^-126 flush to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // NTQ: n-tiles of query columns (1: at most 4 heads, 2: at most 8).
 template <int D, int NTQ>
-__global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(const AttnArgs a) {
   constexpr int J = D / 32;
   using Lay = AttnLayout<D>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -291,10 +299,10 @@ __global__ void __launch_bounds__(kAttnThreads, 3) attn_kernel(const AttnArgs a)
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
         }
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float corr0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-        const float corr1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-        const float p0 = v0 ? exp2f(sc0 - mn0) : 0.f, p1 = v0 ? exp2f(sc1 - mn1) : 0.f;
-        const float p2 = v1 ? exp2f(sc2 - mn0) : 0.f, p3 = v1 ? exp2f(sc3 - mn1) : 0.f;
+        const float corr0 = mn0 == -INFINITY ? 1.f : ex2_approx(m0 - mn0);
+        const float corr1 = mn1 == -INFINITY ? 1.f : ex2_approx(m1 - mn1);
+        const float p0 = v0 ? ex2_approx(sc0 - mn0) : 0.f, p1 = v0 ? ex2_approx(sc1 - mn1) : 0.f;
+        const float p2 = v1 ? ex2_approx(sc2 - mn0) : 0.f, p3 = v1 ? ex2_approx(sc3 - mn1) : 0.f;
         l0 = l0 * corr0 + (p0 + p2);
         l1 = l1 * corr1 + (p1 + p3);
         m0 = mn0;

@@ -386,18 +386,25 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a) {
         const int e = tid + kCW * 32 * j;
         col[j] = e < items ? e : -1;  // float4 index n * kRecCols + c4 of the record
       }
+      // kSP splits per round: their loads are in flight together, then added
+      // in split order
+      constexpr int kSP = NT == 1 ? 1 : 2;
       const float4* rec4 = reinterpret_cast<const float4*>(part_rb);
       const size_t step = a.rec_floats / 4;
-      for (int s0 = 0; s0 < a.S; ++s0) {
-        float4 v[kJ];
+      for (int s0 = 0; s0 < a.S; s0 += kSP) {
+        float4 v[kSP][kJ];
 #pragma unroll
-        for (int j = 0; j < kJ; ++j)
-          if (col[j] >= 0) v[j] = __ldcg(rec4 + (size_t)s0 * step + col[j]);
+        for (int q = 0; q < kSP; ++q)
 #pragma unroll
-        for (int j = 0; j < kJ; ++j)
-          if (col[j] >= 0) {
-            s4[j].x += v[j].x; s4[j].y += v[j].y; s4[j].z += v[j].z; s4[j].w += v[j].w;
-          }
+          for (int j = 0; j < kJ; ++j)
+            if (col[j] >= 0 && s0 + q < a.S) v[q][j] = __ldcg(rec4 + (size_t)(s0 + q) * step + col[j]);
+#pragma unroll
+        for (int q = 0; q < kSP; ++q)
+#pragma unroll
+          for (int j = 0; j < kJ; ++j)
+            if (col[j] >= 0 && s0 + q < a.S) {
+              s4[j].x += v[q][j].x; s4[j].y += v[q][j].y; s4[j].z += v[q][j].z; s4[j].w += v[q][j].w;
+            }
       }
 #pragma unroll
       for (int j = 0; j < kJ; ++j)
