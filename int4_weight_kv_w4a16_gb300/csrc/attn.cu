@@ -576,8 +576,11 @@ AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int f
   // context ranges per (sequence, kv-head, head sub-group): fewest waves of
   // resident CTAs x tiles per range (+ the merge), within the cluster limit
   // and the tiles
+  // (85 % of the resident slots: with programmatic launch the previous
+  // kernel's last CTAs still hold part of the SMs when these start, so a
+  // grid that exactly fills the slots runs as two waves)
   const long long pairs = (long long)batch * s.n_kv_heads * attn_nsub(G);
-  const long long slots = (long long)n_sm * (fit > 0 ? fit : 1);
+  const long long slots = (long long)(0.85 * n_sm * (fit > 0 ? fit : 1));
   const int tiles = (cap + kTilePos - 1) / kTilePos;
   int nc = 1;
   double best = 1e30;
