@@ -59,20 +59,36 @@ struct HeadPre {
 // hpos[task].  Item i = (task, lane) for i = first, first + stride, ...
 __device__ __forceinline__ void fill_head_cache(const ProjArgs& a, int rb, float2* hcs, int* hpos, int first,
                                                 int stride) {
-  const int hpr = kRowsPerBlock / a.d, ntask = a.batch * hpr, half = a.d / 2;
-  for (int i = first; i < ntask * 32; i += stride) {
-    const int task = i >> 5, l = i & 31;
-    const int n = task / hpr, hg = rb * hpr + task % hpr;
-    const int p = a.pos[n];
-    float2 c0 = make_float2(1.f, 0.f), c1 = c0;
-    if (hg < a.Hq + a.Hkv) {  // q and k heads are rotated by position
-      const int pp = p >= 0 && p < a.kv.cap ? p : 0;
-      c0 = a.rope[(size_t)pp * half + l];
-      if (half > 32) c1 = a.rope[(size_t)pp * half + l + 32];
+  const int hpr = kRowsPerBlock / a.d, total = a.batch * hpr * 32, half = a.d / 2;
+  // four items per round: their position loads, then their table loads, are
+  // in flight together
+  for (int i0 = first; i0 < total; i0 += 4 * stride) {
+    int p[4];
+    float2 c0[4], c1[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * stride;
+      p[u] = i < total ? a.pos[(i >> 5) / hpr] : 0;
     }
-    hcs[(task * 2) * 32 + l] = c0;
-    hcs[(task * 2 + 1) * 32 + l] = c1;
-    if (l == 0) hpos[task] = p;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * stride, task = i >> 5, l = i & 31;
+      c0[u] = c1[u] = make_float2(1.f, 0.f);
+      if (i < total && rb * hpr + task % hpr < a.Hq + a.Hkv) {  // q and k heads are rotated by position
+        const int pp = p[u] >= 0 && p[u] < a.kv.cap ? p[u] : 0;
+        c0[u] = a.rope[(size_t)pp * half + l];
+        if (half > 32) c1[u] = a.rope[(size_t)pp * half + l + 32];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * stride, task = i >> 5, l = i & 31;
+      if (i < total) {
+        hcs[(task * 2) * 32 + l] = c0[u];
+        hcs[(task * 2 + 1) * 32 + l] = c1[u];
+        if (l == 0) hpos[task] = p[u];
+      }
+    }
   }
 }
 
