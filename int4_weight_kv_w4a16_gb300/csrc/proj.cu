@@ -29,6 +29,8 @@
 //     QKV   : r * acc, RoPE(q, k) at pos, fp32 Hadamard rotation; q -> fp32
 //             rotated query; k, v -> INT4 + fp16 scale into cache slot pos
 //             (direct KV-cache placement, abstract).
+#include <cuda.h>
+
 #include "futr_internal.cuh"
 #include "proj.cuh"
 
@@ -142,6 +144,191 @@ __device__ __forceinline__ void issue_tile(const ProjArgs& a, uint8_t* stage, in
   for (int n = 0; n < a.batch; ++n) bulk_g2s(dst + n * (kTileLd * 2), src + (size_t)n * a.K, kGroup * 2, bar);
 }
 
+// Everything after the K-loop: the epilogue tile (filled by write_red from
+// the caller's accumulators), the split record and arrival, the last CTA's
+// reduction and the fused epilogue.  Consumer threads only.
+template <int NT, int EPI, class WriteRed>
+__device__ __forceinline__ void proj_tail(const ProjArgs& a, uint8_t* smem, int rb, int sk, float* ss, int* flag,
+                                          bool ok, WriteRed&& write_red) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* red = reinterpret_cast<float*>(smem);  // epilogue [NT*8][kRedLd], aliases the stages
+  // the residual rows of this block (RESID): with one batch tile loaded now,
+  // overlapping the split handshake; with more, in one burst after the
+  // reduction, which keeps them out of its registers
+  constexpr bool kEarly = NT == 1;
+  __nv_bfloat16 rres[EPI == kEpiResid ? NT * 8 : 1];
+  auto load_resid = [&]() {
+    if (EPI == kEpiResid) {
+#pragma unroll
+      for (int n = 0; n < NT * 8; ++n)
+        rres[n] = n < a.batch ? a.resid[(size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid]
+                              : __float2bfloat16_rn(0.f);
+    }
+  };
+  if (kEarly) load_resid();
+  // QKV: the head tasks' positions and RoPE factors go to shared memory after
+  // the epilogue tile and the split-sum groups (the ring is free by then)
+  float2* hcs = reinterpret_cast<float2*>(red + NT * 8 * kRedLd + 4 * kCW * 32);
+  int* hpos = reinterpret_cast<int*>(hcs + a.batch * (kRowsPerBlock / a.d) * 64);
+  if (!ok) {
+    set_err(a.err, FUTR_ERR_TIMEOUT);
+    flag[1] = 1;
+  }
+
+  // ------------------------------------------------------------ epilogue --
+  consumer_sync();  // every warp is done with the stage ring: reuse it as `red`
+  if (flag[1]) return;  // a wait ran out: the ring may still be in use, write nothing
+  write_red(red);
+  consumer_sync();
+
+  if (a.S > 1) {
+    // publish this split's partial record: per batch row 32 float4 of sums and
+    // one float4 (sum of squares, 0, 0, 0); then count arrivals
+    float* rec = a.part + ((size_t)rb * a.S + sk) * a.rec_floats;
+    const int items = a.batch * kRecCols;
+    for (int e = tid; e < items; e += kCW * 32) {
+      const int n = e / kRecCols, c4 = e - kRecCols * n;
+      const float4 v = c4 < 32 ? reinterpret_cast<const float4*>(red + n * kRedLd)[c4]
+                               : make_float4(EPI != kEpiResid ? ss[n] : 0.f, 0.f, 0.f, 0.f);
+      reinterpret_cast<float4*>(rec + n * kRecLd)[c4] = v;
+    }
+    consumer_sync();
+    if (tid == 0)
+      flag[0] = atom_add_acq_rel_gpu(&a.cnt[rb], 1u) == (unsigned)(a.S - 1) ? 1 : 0;
+    else if (EPI == kEpiQkv)
+      fill_head_cache(a, rb, hcs, hpos, tid - 1, kCW * 32 - 1);  // overlaps the arrival
+    consumer_sync();
+    if (!flag[0]) return;
+    // The last CTA adds the S records.  With few columns (small batch), G
+    // groups of threads each add a contiguous range of splits, all loads of a
+    // range in flight together; the G group sums are then added in group
+    // order.  The order is fixed, so the result is deterministic.
+    const int G = items >= kCW * 32 ? 1 : (kCW * 32) / items;
+    float4* gsum = reinterpret_cast<float4*>(red + NT * 8 * kRedLd);  // [G][items], G > 1 only
+    const float* part_rb = a.part + (size_t)rb * a.S * a.rec_floats;
+    if (G == 1) {
+      // Many columns (batch >= 4): thread t owns columns t + 128 j and adds
+      // them split by split, the loads of all its columns for one split in
+      // flight together (the sum of each column stays in split order).
+      constexpr int kJ = (NT * 8 * kRecCols + kCW * 32 - 1) / (kCW * 32);
+      float4 s4[kJ];
+      int col[kJ];
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        s4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int e = tid + kCW * 32 * j;
+        col[j] = e < items ? e : -1;  // float4 index n * kRecCols + c4 of the record
+      }
+      // kSP splits per round: their loads are in flight together, then added
+      // in split order
+      constexpr int kSP = NT == 1 ? 1 : 2;
+      const float4* rec4 = reinterpret_cast<const float4*>(part_rb);
+      const size_t step = a.rec_floats / 4;
+      for (int s0 = 0; s0 < a.S; s0 += kSP) {
+        float4 v[kSP][kJ];
+#pragma unroll
+        for (int q = 0; q < kSP; ++q)
+#pragma unroll
+          for (int j = 0; j < kJ; ++j)
+            if (col[j] >= 0 && s0 + q < a.S) v[q][j] = __ldcg(rec4 + (size_t)(s0 + q) * step + col[j]);
+#pragma unroll
+        for (int q = 0; q < kSP; ++q)
+#pragma unroll
+          for (int j = 0; j < kJ; ++j)
+            if (col[j] >= 0 && s0 + q < a.S) {
+              s4[j].x += v[q][j].x; s4[j].y += v[q][j].y; s4[j].z += v[q][j].z; s4[j].w += v[q][j].w;
+            }
+      }
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        if (col[j] >= 0) {
+          const int n = col[j] / kRecCols, c4 = col[j] - kRecCols * n;
+          if (c4 < 32)
+            reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4[j];
+          else
+            ss[n] = s4[j].x;
+        }
+    }
+    for (int t = tid; G > 1 && t < G * items; t += kCW * 32) {
+      const int grp = t / items, e = t - grp * items;
+      const int n = e / kRecCols, c4 = e - kRecCols * n;
+      const int s_lo = grp * a.S / G, s_hi = (grp + 1) * a.S / G;
+      const float4* src = reinterpret_cast<const float4*>(part_rb + n * kRecLd) + c4;
+      float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = s_lo; s0 < s_hi; s0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j < s_hi) v[j] = __ldcg(src + (size_t)(s0 + j) * (a.rec_floats / 4));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (s0 + j < s_hi) {
+            s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
+          }
+      }
+      gsum[t] = s4;
+    }
+    if (G > 1) {
+      consumer_sync();
+      for (int e = tid; e < items; e += kCW * 32) {
+        float4 s4 = gsum[e];
+        for (int grp = 1; grp < G; ++grp) {
+          const float4 v = gsum[grp * items + e];
+          s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
+        }
+        const int n = e / kRecCols, c4 = e - kRecCols * n;
+        if (c4 < 32)
+          reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4;
+        else
+          ss[n] = s4.x;
+      }
+    }
+    if (tid == 0) a.cnt[rb] = 0u;  // self-reset for the next launch
+    consumer_sync();
+  }
+
+  if (!kEarly) load_resid();
+  if (EPI == kEpiQkv && a.S == 1) {
+    fill_head_cache(a, rb, hcs, hpos, tid, kCW * 32);
+    consumer_sync();
+  }
+  if (EPI == kEpiResid) {
+    // consumer thread t owns output row t of the block (kCW * 32 == 128)
+#pragma unroll
+    for (int n = 0; n < NT * 8; ++n)
+      if (n < a.batch) {
+        const size_t o = (size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid;
+        a.out[o] = __float2bfloat16_rn(__bfloat162float(rres[n]) + red[n * kRedLd + tid]);
+      }
+  } else if (EPI == kEpiSwiglu) {
+    for (int e = tid; e < a.batch * 64; e += kCW * 32) {
+      const int n = e >> 6, r = e & 63;
+      const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(ss[n], (float)a.K) + a.eps));
+      const float g = rn * red[n * kRedLd + r];
+      const float u = rn * red[n * kRedLd + 64 + r];
+      const float sg = __fdiv_rn(g, 1.0f + expf(-g));
+      a.out[(size_t)n * a.out_ld + (size_t)rb * 64 + r] = __float2bfloat16_rn(sg * u);
+    }
+  } else {
+    if (rb == 0 && tid == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
+      set_err(a.err, FUTR_ERR_BAD_BLOB);
+    const int hpr = kRowsPerBlock / a.d;
+    for (int task = warp; task < a.batch * hpr; task += kCW) {
+      const int n = task / hpr, hl = task % hpr;
+      const int hg = rb * hpr + hl;
+      const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(ss[n], (float)a.K) + a.eps));
+      HeadPre hp;
+      hp.p = hpos[task];
+      hp.cs[0] = hcs[(task * 2) * 32 + lane];
+      hp.cs[1] = hcs[(task * 2 + 1) * 32 + lane];
+      if (a.d == 128)
+        qkv_head_epilogue<4>(a, red, n, hl, hg, rn, hp);
+      else
+        qkv_head_epilogue<2>(a, red, n, hl, hg, rn, hp);
+    }
+  }
+}
+
 template <int NT, int EPI>
 __device__ __forceinline__ void proj_body(const ProjArgs& a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -156,7 +343,6 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a) {
   int* flag = reinterpret_cast<int*>(ss + 32);                // [4]
   uint64_t* full = reinterpret_cast<uint64_t*>(flag + 4);
   uint64_t* empty = full + kMaxRing;
-  float* red = reinterpret_cast<float*>(smem);  // epilogue [NT*8][kRedLd], aliases the stages
 
   if (tid == 0) {
     flag[0] = 0;
@@ -321,33 +507,8 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a) {
       if ((tid & 15) == 0 && n < a.batch) ss[n] = ssq[p];
     }
   }
-  // the residual rows of this block (RESID): with one batch tile loaded now,
-  // overlapping the split handshake; with more, in one burst after the
-  // reduction, which keeps them out of its registers
-  constexpr bool kEarly = NT == 1;
-  __nv_bfloat16 rres[EPI == kEpiResid ? NT * 8 : 1];
-  auto load_resid = [&]() {
-    if (EPI == kEpiResid) {
-#pragma unroll
-      for (int n = 0; n < NT * 8; ++n)
-        rres[n] = n < a.batch ? a.resid[(size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid]
-                              : __float2bfloat16_rn(0.f);
-    }
-  };
-  if (kEarly) load_resid();
-  // QKV: the head tasks' positions and RoPE factors go to shared memory after
-  // the epilogue tile and the split-sum groups (the ring is free by then)
-  float2* hcs = reinterpret_cast<float2*>(red + NT * 8 * kRedLd + 4 * kCW * 32);
-  int* hpos = reinterpret_cast<int*>(hcs + a.batch * (kRowsPerBlock / a.d) * 64);
-  if (!ok) {
-    set_err(a.err, FUTR_ERR_TIMEOUT);
-    flag[1] = 1;
-  }
-
-  // ------------------------------------------------------------ epilogue --
-  consumer_sync();  // every warp is done with the stage ring: reuse it as `red`
-  if (flag[1]) return;  // a wait ran out: the ring may still be in use, write nothing
-  {
+  // accumulator fragments -> epilogue tile [batch row][block row]
+  proj_tail<NT, EPI>(a, smem, rb, sk, ss, flag, ok, [&](float* red) {
     const int t = lane & 3;
 #pragma unroll
     for (int m = 0; m < kMT; ++m) {
@@ -361,155 +522,352 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a) {
         red[(n0 + 1) * kRedLd + r0 + 8] = acc[m][nt][3];
       }
     }
-  }
-  consumer_sync();
+  });
+}
 
-  if (a.S > 1) {
-    // publish this split's partial record: per batch row 32 float4 of sums and
-    // one float4 (sum of squares, 0, 0, 0); then count arrivals
-    float* rec = a.part + ((size_t)rb * a.S + sk) * a.rec_floats;
-    const int items = a.batch * kRecCols;
-    for (int e = tid; e < items; e += kCW * 32) {
-      const int n = e / kRecCols, c4 = e - kRecCols * n;
-      const float4 v = c4 < 32 ? reinterpret_cast<const float4*>(red + n * kRedLd)[c4]
-                               : make_float4(EPI != kEpiResid ? ss[n] : 0.f, 0.f, 0.f, 0.f);
-      reinterpret_cast<float4*>(rec + n * kRecLd)[c4] = v;
+// ------------------------------------------------- tensor-core variant --
+// Batch 17..32: the same unit stream and epilogue, with the products on the
+// 5th-generation tensor cores.  Per unit (128 rows x 128 inputs):
+//   warps 0..3 unpack their 32 rows' codes into bf16 MMA fragments (the same
+//     registers the mma.sync path feeds) and store them to tensor memory with
+//     tcgen05.st.16x128b.x2, which lays a 16-row fragment of one k-step out as
+//     16 lanes x 8 columns in natural k order: A = 128 lanes (rows) x 64
+//     columns (bf16 pairs);
+//   warps 5 and 6 (one thread each) issue the 8 tcgen05.mma kind::f16 (M 128,
+//     N 32, K 16) of the even and the odd units: A from tensor memory, B = the
+//     activation tile in shared memory (K-major, two boxes of 32 rows x 64
+//     inputs written by 2-D tensor copies with the 128-byte swizzle, read
+//     through a 128-byte-swizzle descriptor), D = fp32 in tensor memory,
+//     then tcgen05.commit signals the consumers and frees the ring slot.  An
+//     issuing thread is held ~60 ns per MMA whatever N is (measured), while
+//     issuers in different warps overlap: two issuers halve the cost;
+//   warps 0..3 read D back two units later (tcgen05.ld.32x32b: thread = row,
+//     32 batch columns), multiply by the row's group scale and add into
+//     registers.
+// A has three buffers and D two (256 tensor-memory columns per CTA, two CTAs
+// per SM), so the unpacking of unit i, the MMAs of units i - 1 and i - 2 and
+// the read-back of unit i - 2 overlap.  Every wait is bounded; tensor memory
+// is freed before the epilogue, once both issuers are past their last MMA
+// (and, after a time-out, their last commits have landed).  Used for the
+// residual and SwiGLU epilogues (see plan_projection).
+constexpr int kTcCols = 256;                       // tensor-memory columns per CTA
+constexpr int kTcA = 0;                            // A[b], b < 3: columns 64 b .. 64 b + 63
+constexpr int kTcD = 192;                          // D[b], b < 2: columns 192 + 32 b .. + 31
+constexpr int kTcTile = 32 * kGroup * 2;           // activation tile: 32 rows x 128 inputs, bf16
+constexpr int kTcStage = 17 * 1024;                // tile (8 KB) + weight unit (8448 B), padded to 1 KB
+constexpr int kTcThreads = (kCW + 3) * 32;         // consumers, producer, two MMA issuers
+constexpr int kTcMisc = 32 * 4 + 16 + (2 * kMaxRing + 5) * 8 + 32;
+// instruction descriptor: D f32, A and B bf16, both K-major, N = 32, M = 128
+constexpr uint32_t kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// shared-memory operand descriptor, K-major with the 128-byte swizzle: rows of
+// 128 bytes in 8-row atoms of 1 KB (sbo = 1024); a k-step starts 32 bytes
+// further along the row
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(kTcIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_st_frag(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_ld_row32(uint32_t taddr, float (&v)[32]) {
+  uint32_t u[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]), "=r"(u[8]),
+        "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]), "=r"(u[16]),
+        "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]),
+        "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
+}
+
+__device__ __forceinline__ void tma_2d_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// activation tile of group g: inputs 128 g .. 128 g + 127 as two 4 KB boxes
+__device__ __forceinline__ void tc_issue_tile(uint8_t* dst, const CUtensorMap* map, int g, uint64_t* bar) {
+  tma_2d_box(dst, map, kGroup * g, 0, bar);
+  tma_2d_box(dst + 4096, map, kGroup * g + 64, 0, bar);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    proj_tc_kernel(const __grid_constant__ ProjArgs a, const __grid_constant__ CUtensorMap xmap) {
+  constexpr int NT = 4;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rb = blockIdx.x / a.S, sk = blockIdx.x - rb * a.S;
+  const int g0 = (int)(((long long)sk * a.n_groups) / a.S);
+  const int g1 = (int)(((long long)(sk + 1) * a.n_groups) / a.S);
+  const int ng = g1 - g0, R = a.ring;
+
+  uint8_t* stages = smem;
+  float* ss = reinterpret_cast<float*>(smem + a.off_misc);  // [32] sum of squares per batch row
+  int* flag = reinterpret_cast<int*>(ss + 32);                // [4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(flag + 4);
+  uint64_t* empty = full + kMaxRing;   // released by the MMA commit of the slot's unit
+  uint64_t* aready = empty + kMaxRing; // [3] the 4 consumer warps stored A[b] (and read D two units back)
+  uint64_t* mdone = aready + 3;        // [2] the MMAs into D[b] (and their reads of A) completed
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(mdone + 2);
+  int* last_issued = reinterpret_cast<int*>(tbase + 1);  // [2] per issuer
+  int* issuers_done = last_issued + 2;
+
+  if (tid == 0) {
+    flag[0] = 0;
+    flag[1] = 0;
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
-    consumer_sync();
-    if (tid == 0)
-      flag[0] = atom_add_acq_rel_gpu(&a.cnt[rb], 1u) == (unsigned)(a.S - 1) ? 1 : 0;
-    else if (EPI == kEpiQkv)
-      fill_head_cache(a, rb, hcs, hpos, tid - 1, kCW * 32 - 1);  // overlaps the arrival
-    consumer_sync();
-    if (!flag[0]) return;
-    // The last CTA adds the S records.  With few columns (small batch), G
-    // groups of threads each add a contiguous range of splits, all loads of a
-    // range in flight together; the G group sums are then added in group
-    // order.  The order is fixed, so the result is deterministic.
-    const int G = items >= kCW * 32 ? 1 : (kCW * 32) / items;
-    float4* gsum = reinterpret_cast<float4*>(red + NT * 8 * kRedLd);  // [G][items], G > 1 only
-    const float* part_rb = a.part + (size_t)rb * a.S * a.rec_floats;
-    if (G == 1) {
-      // Many columns (batch >= 4): thread t owns columns t + 128 j and adds
-      // them split by split, the loads of all its columns for one split in
-      // flight together (the sum of each column stays in split order).
-      constexpr int kJ = (NT * 8 * kRecCols + kCW * 32 - 1) / (kCW * 32);
-      float4 s4[kJ];
-      int col[kJ];
-#pragma unroll
-      for (int j = 0; j < kJ; ++j) {
-        s4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int e = tid + kCW * 32 * j;
-        col[j] = e < items ? e : -1;  // float4 index n * kRecCols + c4 of the record
+    for (int b = 0; b < 3; ++b) mbar_init(&aready[b], kCW);
+    for (int b = 0; b < 2; ++b) mbar_init(&mdone[b], 1);
+    last_issued[0] = last_issued[1] = -1;
+    *issuers_done = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tbase)),
+                 "r"(kTcCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tbase;
+  pdl_trigger();
+
+  const uint8_t* unit0 = a.w + ((size_t)rb * a.n_groups + g0) * kUnitBytes;
+  if (warp == kCW) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      const uint32_t tx = kUnitBytes + kTcTile;
+      const int pre = ng < R ? ng : R;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], tx);
+        bulk_g2s(stages + (size_t)i * kTcStage + kTcTile, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[i]);
       }
-      // kSP splits per round: their loads are in flight together, then added
-      // in split order
-      constexpr int kSP = NT == 1 ? 1 : 2;
-      const float4* rec4 = reinterpret_cast<const float4*>(part_rb);
-      const size_t step = a.rec_floats / 4;
-      for (int s0 = 0; s0 < a.S; s0 += kSP) {
-        float4 v[kSP][kJ];
-#pragma unroll
-        for (int q = 0; q < kSP; ++q)
-#pragma unroll
-          for (int j = 0; j < kJ; ++j)
-            if (col[j] >= 0 && s0 + q < a.S) v[q][j] = __ldcg(rec4 + (size_t)(s0 + q) * step + col[j]);
-#pragma unroll
-        for (int q = 0; q < kSP; ++q)
-#pragma unroll
-          for (int j = 0; j < kJ; ++j)
-            if (col[j] >= 0 && s0 + q < a.S) {
-              s4[j].x += v[q][j].x; s4[j].y += v[q][j].y; s4[j].z += v[q][j].z; s4[j].w += v[q][j].w;
-            }
-      }
-#pragma unroll
-      for (int j = 0; j < kJ; ++j)
-        if (col[j] >= 0) {
-          const int n = col[j] / kRecCols, c4 = col[j] - kRecCols * n;
-          if (c4 < 32)
-            reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4[j];
-          else
-            ss[n] = s4[j].x;
+      pdl_wait();  // the activations come from the previous kernel
+      const unsigned long long deadline = global_ns() + kWaitNs;
+      for (int i = 0; i < pre; ++i) tc_issue_tile(stages + (size_t)i * kTcStage, &xmap, g0 + i, &full[i]);
+      int slot = 0;
+      uint32_t phase = 0;
+      for (int i = R; i < ng; ++i) {
+        if (!mbar_wait_until(&empty[slot], phase, deadline)) {
+          set_err(a.err, FUTR_ERR_TIMEOUT);
+          break;
         }
+        uint8_t* st = stages + (size_t)slot * kTcStage;
+        mbar_arrive_expect_tx(&full[slot], tx);
+        bulk_g2s(st + kTcTile, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[slot]);
+        tc_issue_tile(st, &xmap, g0 + i, &full[slot]);
+        if (++slot == R) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    } else {
+      pdl_wait();
     }
-    for (int t = tid; G > 1 && t < G * items; t += kCW * 32) {
-      const int grp = t / items, e = t - grp * items;
-      const int n = e / kRecCols, c4 = e - kRecCols * n;
-      const int s_lo = grp * a.S / G, s_hi = (grp + 1) * a.S / G;
-      const float4* src = reinterpret_cast<const float4*>(part_rb + n * kRecLd) + c4;
-      float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = s_lo; s0 < s_hi; s0 += 8) {
-        float4 v[8];
+    return;
+  }
+
+  if (warp > kCW) {
+    // ----------------------------------------------------- MMA issuers --
+    // warp kCW + 1 + b issues units i = b, b + 2, ... into D[b]
+    const int b = warp - kCW - 1;
+    if (lane == 0) {
+      const unsigned long long deadline = global_ns() + kWaitNs;
+      bool ok = true;
+      for (int i = b; i < ng; i += 2) {
+        const int slot = i % R, ba = i % 3;
+        // the tile has landed; the four consumer warps stored A(i) and read
+        // D(i - 2), the previous contents of D[b]
+        if (!mbar_wait_until(&full[slot], (uint32_t)(i / R) & 1u, deadline) ||
+            !mbar_wait_until(&aready[ba], (uint32_t)(i / 3) & 1u, deadline)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tile = smem_u32(stages + (size_t)slot * kTcStage);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (s0 + j < s_hi) v[j] = __ldcg(src + (size_t)(s0 + j) * (a.rec_floats / 4));
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma(tm + kTcD + 32 * b, tm + kTcA + 64 * ba + 8 * ks,
+                 tc_desc_sw128(tile + 4096 * (ks >> 2) + 32 * (ks & 3)), ks > 0);
+        tc_commit(&mdone[b]);
+        tc_commit(&empty[slot]);  // the ring slot is free once these MMAs have read the tile
+        last_issued[b] = i;
+      }
+      if (!ok) {
+        set_err(a.err, FUTR_ERR_TIMEOUT);
+        flag[1] = 1;
+      }
+      __threadfence_block();
+      atomicAdd(issuers_done, 1);  // no MMA of this warp is issued after this point
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- consumers --
+  pdl_wait();
+  const unsigned long long deadline = global_ns() + kWaitNs;
+  bool ok = true;
+  float acc[32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (s0 + j < s_hi) {
-            s4.x += v[j].x; s4.y += v[j].y; s4.z += v[j].z; s4.w += v[j].w;
+  for (int n = 0; n < 32; ++n) acc[n] = 0.f;
+  // RMSNorm sum of squares: thread t squares one 16-byte chunk of tile row
+  // n = t / 16 + 8p, box (t % 16) / 8, stored chunk t % 8 (which inputs the
+  // chunk holds under the swizzle does not matter for the sum); bytes
+  const int sq_off = ((tid & 15) >> 3) * 4096 + (tid >> 4) * 128 + (tid & 7) * 16;
+  float ssq[NT];
+#pragma unroll
+  for (int p = 0; p < NT; ++p) ssq[p] = 0.f;
+  const uint32_t lq = (uint32_t)(32 * warp) << 16;  // this warp's lane quarter
+  const int row = 32 * warp + lane;                  // block row of this thread's D lane
+  float s1 = 0.f, s2 = 0.f;  // group scales of units i - 1 and i - 2 for this row
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int i = 0; i < ng + 2; ++i) {
+    float s0 = 0.f;
+    if (i < ng) {
+      const uint8_t* st = stages + (size_t)slot * kTcStage;
+      const int ba = i % 3;
+      if (!mbar_wait_until(&full[slot], phase, deadline)) {
+        ok = false;
+        break;
+      }
+      const uint4* wt = reinterpret_cast<const uint4*>(st + kTcTile + kMT * warp * 1024);
+      s0 = __half2float(reinterpret_cast<const __half*>(st + kTcTile + kUnitCodeBytes)[row]);
+      uint32_t words[kMT][8];
+#pragma unroll
+      for (int m = 0; m < kMT; ++m) {
+        const uint4 w0 = wt[64 * m + lane], w1 = wt[64 * m + 32 + lane];
+        words[m][0] = w0.x; words[m][1] = w0.y; words[m][2] = w0.z; words[m][3] = w0.w;
+        words[m][4] = w1.x; words[m][5] = w1.y; words[m][6] = w1.z; words[m][7] = w1.w;
+      }
+      // A[ba] was last read by the MMAs of unit i - 3, whose completion this
+      // warp waited for before reading D of that unit
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int m = 0; m < kMT; ++m) {
+          uint32_t af[4];
+          nib4_bf16x2(words[m][ks], af);
+          tc_st_frag(tm + lq + ((uint32_t)(16 * m) << 16) + kTcA + 64 * ba + 8 * ks, af);
+        }
+      if (EPI != kEpiResid) {
+#pragma unroll
+        for (int p = 0; p < NT; ++p)
+          if ((tid >> 4) + 8 * p < a.batch) {
+            const uint4 v = *reinterpret_cast<const uint4*>(st + sq_off + 1024 * p);
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = __uint_as_float(u[j] << 16), hi = __uint_as_float(u[j] & 0xffff0000u);
+              ssq[p] = fmaf(lo, lo, fmaf(hi, hi, ssq[p]));
+            }
           }
       }
-      gsum[t] = s4;
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     }
-    if (G > 1) {
-      consumer_sync();
-      for (int e = tid; e < items; e += kCW * 32) {
-        float4 s4 = gsum[e];
-        for (int grp = 1; grp < G; ++grp) {
-          const float4 v = gsum[grp * items + e];
-          s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
-        }
-        const int n = e / kRecCols, c4 = e - kRecCols * n;
-        if (c4 < 32)
-          reinterpret_cast<float4*>(red + n * kRedLd)[c4] = s4;
-        else
-          ss[n] = s4.x;
+    if (i >= 2) {
+      // D of unit i - 2; its buffer is overwritten by the MMAs of unit i,
+      // which wait for this warp's arrival below
+      const int v = i - 2, bd = v & 1;
+      if (!mbar_wait_until(&mdone[bd], (uint32_t)(v >> 1) & 1u, deadline)) {
+        ok = false;
+        break;
       }
-    }
-    if (tid == 0) a.cnt[rb] = 0u;  // self-reset for the next launch
-    consumer_sync();
-  }
-
-  if (!kEarly) load_resid();
-  if (EPI == kEpiQkv && a.S == 1) {
-    fill_head_cache(a, rb, hcs, hpos, tid, kCW * 32);
-    consumer_sync();
-  }
-  if (EPI == kEpiResid) {
-    // consumer thread t owns output row t of the block (kCW * 32 == 128)
+      tc_fence_after();
+      float d[32];
+      tc_ld_row32(tm + lq + kTcD + 32 * bd, d);
 #pragma unroll
-    for (int n = 0; n < NT * 8; ++n)
-      if (n < a.batch) {
-        const size_t o = (size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid;
-        a.out[o] = __float2bfloat16_rn(__bfloat162float(rres[n]) + red[n * kRedLd + tid]);
-      }
-  } else if (EPI == kEpiSwiglu) {
-    for (int e = tid; e < a.batch * 64; e += kCW * 32) {
-      const int n = e >> 6, r = e & 63;
-      const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(ss[n], (float)a.K) + a.eps));
-      const float g = rn * red[n * kRedLd + r];
-      const float u = rn * red[n * kRedLd + 64 + r];
-      const float sg = __fdiv_rn(g, 1.0f + expf(-g));
-      a.out[(size_t)n * a.out_ld + (size_t)rb * 64 + r] = __float2bfloat16_rn(sg * u);
+      for (int n = 0; n < 32; ++n) acc[n] = fmaf(s2, d[n], acc[n]);
     }
-  } else {
-    if (rb == 0 && tid == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
-      set_err(a.err, FUTR_ERR_BAD_BLOB);
-    const int hpr = kRowsPerBlock / a.d;
-    for (int task = warp; task < a.batch * hpr; task += kCW) {
-      const int n = task / hpr, hl = task % hpr;
-      const int hg = rb * hpr + hl;
-      const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(ss[n], (float)a.K) + a.eps));
-      HeadPre hp;
-      hp.p = hpos[task];
-      hp.cs[0] = hcs[(task * 2) * 32 + lane];
-      hp.cs[1] = hcs[(task * 2 + 1) * 32 + lane];
-      if (a.d == 128)
-        qkv_head_epilogue<4>(a, red, n, hl, hg, rn, hp);
-      else
-        qkv_head_epilogue<2>(a, red, n, hl, hg, rn, hp);
+    if (i < ng) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aready[i % 3]);  // A(i) stored, D(i - 2) read
+      if (++slot == R) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    s2 = s1;
+    s1 = s0;
+  }
+  if (!ok) {
+    set_err(a.err, FUTR_ERR_TIMEOUT);
+    flag[1] = 1;
+  }
+  consumer_sync();
+  if (warp == 0) {
+    // tensor memory is freed once the last issued MMAs have landed (already
+    // waited for on the normal path; bounded here for a path that timed out)
+    // both issuers are past their last MMA (bounded wait); on the normal path
+    // every MMA has completed already (all units' D were read back), after a
+    // time-out the issuers' last commits are waited for
+    if (lane == 0) {
+      const unsigned long long dl = global_ns() + kWaitNs;
+      while (*(volatile int*)issuers_done < 2 && global_ns() < dl) {
+      }
+      __threadfence_block();
+    }
+    __syncwarp();
+    if (lane < 2 && flag[1]) {
+      const int v = *(volatile int*)&last_issued[lane];
+      if (v >= 0 && !mbar_wait_until(&mdone[lane], (uint32_t)(v >> 1) & 1u, global_ns() + kWaitNs))
+        set_err(a.err, FUTR_ERR_TIMEOUT);
+    }
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(kTcCols) : "memory");
+  }
+  if (EPI != kEpiResid) {
+#pragma unroll
+    for (int p = 0; p < NT; ++p) {
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) ssq[p] += __shfl_xor_sync(0xffffffffu, ssq[p], o);
+      const int n = (tid >> 4) + 8 * p;
+      if ((tid & 15) == 0 && n < a.batch) ss[n] = ssq[p];
     }
   }
+  // thread t holds block row t for batch columns 0..31
+  proj_tail<NT, EPI>(a, smem, rb, sk, ss, flag, ok, [&](float* red) {
+#pragma unroll
+    for (int n = 0; n < 32; ++n) red[n * kRedLd + tid] = acc[n];
+  });
 }
 
 template <int NT, int EPI>
@@ -577,6 +935,55 @@ cudaError_t launch_nt(int nt, const ProjArgs& a, int grid, size_t smem, cudaStre
   }
 }
 
+template <int EPI>
+cudaError_t configure_tc(int dev) {
+  static unsigned long long configured = 0;  // one bit per device
+  if (configured & (1ull << (dev & 63))) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kProjMaxSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(proj_tc_kernel<EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  configured |= 1ull << (dev & 63);
+  return cudaSuccess;
+}
+
+template <int EPI>
+cudaError_t launch_tc(const ProjArgs& a, int grid, size_t smem, cudaStream_t st, bool pdl) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = configure_tc<EPI>(dev);
+  if (e != cudaSuccess) return e;
+  CUtensorMap xmap;
+  if (!make_act_tile_map(&xmap, a.xin, a.batch, a.K)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, proj_tc_kernel<EPI>, a, xmap);
+}
+
+int resident_tc(int epi, size_t smem) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  cudaError_t e = cudaSuccess;
+  if (epi == kEpiResid) {
+    e = configure_tc<kEpiResid>(dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_tc_kernel<kEpiResid>, kTcThreads, smem);
+  } else {
+    e = configure_tc<kEpiSwiglu>(dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_tc_kernel<kEpiSwiglu>, kTcThreads, smem);
+  }
+  return e == cudaSuccess ? n : 0;
+}
+
 int resident_ctas(int nt, int epi, size_t smem) {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -602,12 +1009,18 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   p.n_groups = cols / kGroup;
   p.nt = (batch + 7) / 8;
   p.epi = epi;
+  // batch 17..32: the tensor-core kernel (32 batch columns, two CTAs per SM)
+  // for the projections where it measured faster than mma.sync at batch 32
+  // on the 8B and 70B shapes: O and down (residual epilogue) at both, gate/up
+  // only with K >= 8192 (its 8B shape was 10 % slower); QKV stays on mma.sync
+  p.tc = batch > 16 && (epi == kEpiResid || (epi == kEpiSwiglu && p.n_groups >= 64));
+  if (p.tc) p.nt = 4;
   // ring stage = weight unit + activation tile; as deep as lets the target
-  // number of CTAs share an SM (5 up to batch 8, else 3)
-  p.stage_bytes = kUnitBytes + batch * kTileLd * 2;
-  const int misc = 32 * 4 + 16 + 2 * kMaxRing * 8;
-  const int per_sm = batch <= 8 ? 5 : 3;
-  const int budget = 232448 / per_sm - 1024 - misc - 2048;  // per-CTA reserve and static arrays
+  // number of CTAs share an SM (5 up to batch 8, 3 up to 16, 2 beyond)
+  p.stage_bytes = p.tc ? kTcStage : kUnitBytes + batch * kTileLd * 2;
+  const int misc = p.tc ? kTcMisc : 32 * 4 + 16 + 2 * kMaxRing * 8;
+  const int per_sm = batch <= 8 ? 5 : (p.tc ? 2 : 3);
+  const int budget = 232448 / per_sm - 1024 - misc - 2048 - (p.tc ? 1024 : 0);  // reserve, static arrays, alignment
   int ring = budget / p.stage_bytes;
   if (ring > kMaxRing) ring = kMaxRing;
   if (ring < 2) ring = 2;
@@ -618,10 +1031,10 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   const int red_bytes = p.nt * 8 * kRedLd * 4 + kCW * 32 * 16 + (epi == kEpiQkv ? batch * 2 * 512 + 256 : 0);
   if (ring_bytes < red_bytes) ring_bytes = red_bytes;
   p.off_misc = (ring_bytes + 127) & ~127;
-  p.smem = (size_t)p.off_misc + misc;
+  p.smem = (size_t)p.off_misc + misc + (p.tc ? 1024 : 0);  // tc: the base is rounded up to 1024 bytes
   // splits: balance waves of resident CTAs; each extra split costs a partial
   // write and a share of the reduction
-  const int fit = resident_ctas(p.nt, epi, p.smem);
+  const int fit = p.tc ? resident_tc(epi, p.smem) : resident_ctas(p.nt, epi, p.smem);
   const long long slots = (long long)n_sm * (fit > 0 ? fit : 1);
   int best_s = 1;
   double best = 1e30;
@@ -650,6 +1063,10 @@ cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream
   a.off_misc = p.off_misc;
   a.rec_floats = p.rec_floats;
   const int grid = p.n_rb * p.S;
+  if (p.tc) {  // residual and SwiGLU epilogues only
+    if (epi == kEpiResid) return launch_tc<kEpiResid>(a, grid, p.smem, st, pdl);
+    return launch_tc<kEpiSwiglu>(a, grid, p.smem, st, pdl);
+  }
   if (epi == kEpiResid) return launch_nt<kEpiResid>(p.nt, a, grid, p.smem, st, pdl);
   if (epi == kEpiSwiglu) return launch_nt<kEpiSwiglu>(p.nt, a, grid, p.smem, st, pdl);
   return launch_nt<kEpiQkv>(p.nt, a, grid, p.smem, st, pdl);

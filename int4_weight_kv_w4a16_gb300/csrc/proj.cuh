@@ -1,6 +1,8 @@
 // Arguments and launch plans of the W4A16 projection and attention kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "futr_internal.cuh"
 
 namespace futr {
@@ -39,6 +41,7 @@ struct ProjArgs {
 
 struct ProjPlan {
   int n_rb, n_groups, nt, S, epi;
+  bool tc;                       // tensor-core kernel (batch 17..32)
   int ring, stage_bytes, off_misc, rec_floats;
   size_t smem;
   size_t part_floats;
@@ -63,6 +66,10 @@ struct AttnPlan {
   size_t smem;
   size_t part_floats;            // global scratch (none: ranges merge in distributed shared memory)
 };
+
+// Tensor map of a tensor-core projection's activation tiles (defined with the
+// other tensor maps in step.cu).
+bool make_act_tile_map(CUtensorMap* m, const void* x, int rows, int K);
 
 AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int force_split);
 cudaError_t launch_attention(const AttnPlan& p, AttnArgs a, int d, cudaStream_t st, bool pdl);

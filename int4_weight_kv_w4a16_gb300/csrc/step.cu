@@ -285,6 +285,13 @@ cudaError_t launch_final_norm(const uint16_t* y, const float* g, int H, float ep
                     reinterpret_cast<const __nv_bfloat16*>(y), g, H, eps, reinterpret_cast<__nv_bfloat16*>(xg), r);
 }
 
+// Activation tiles of a tensor-core projection: the same 64-input x rows
+// boxes (128-byte swizzle) as the LM head's activation; rows past `rows`
+// read as zero.
+bool make_act_tile_map(CUtensorMap* m, const void* x, int rows, int K) {
+  return make_map(m, x, (uint64_t)K, (uint64_t)rows, 32);
+}
+
 cudaError_t launch_lm_head(const uint16_t* xg, const uint16_t* w, int vocab, int H, int batch, const float* r,
                            float* logits, int* err, cudaStream_t st, bool pdl) {
   const int nt = (batch + 7) / 8;
