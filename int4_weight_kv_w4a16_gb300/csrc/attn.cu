@@ -528,30 +528,36 @@ cudaError_t launch_d(const AttnPlan& p, const AttnArgs& a, cudaStream_t st, bool
 // Largest cluster the device schedules for this kernel (at most kMaxCluster).
 template <int D, int NTQ>
 int max_cluster(size_t smem) {
-  int dev = 0, n = 0;
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || configure_attn<D, NTQ>(dev) != cudaSuccess) return 1;
-  AttnPlan p{};
-  p.NC = 1;
-  p.smem = smem;
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = attn_config(p, 1, 1, 0, attr, false);
-  cfg.numAttrs = 0;  // the query wants no cluster dimension set
-  if (cudaOccupancyMaxPotentialClusterSize(&n, attn_kernel<D, NTQ>, &cfg) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    return 1;
-  }
-  return n < kMaxCluster ? n : kMaxCluster;
+  return remembered(occ_key(dev, D, NTQ, smem), [&]() {
+    int n = 0;
+    AttnPlan p{};
+    p.NC = 1;
+    p.smem = smem;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = attn_config(p, 1, 1, 0, attr, false);
+    cfg.numAttrs = 0;  // the query wants no cluster dimension set
+    if (cudaOccupancyMaxPotentialClusterSize(&n, attn_kernel<D, NTQ>, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return 1;
+    }
+    return n < kMaxCluster ? n : kMaxCluster;
+  });
 }
 
 template <int D, int NTQ>
 int resident_attn(size_t smem) {
-  int dev = 0, n = 0;
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || configure_attn<D, NTQ>(dev) != cudaSuccess) return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, NTQ>, kAttnThreads, smem) != cudaSuccess) {
-    cudaGetLastError();
-    return 1;
-  }
-  return n;
+  return remembered(occ_key(dev, D, NTQ, smem), [&]() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<D, NTQ>, kAttnThreads, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+    return n;
+  });
 }
 
 // The four instantiations, by head dim and query n-tiles.

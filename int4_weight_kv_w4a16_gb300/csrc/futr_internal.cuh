@@ -9,9 +9,35 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <unordered_map>
+
 #include "futr.h"
 
 namespace futr {
+
+// Occupancy answers (CTAs per SM, cluster sizes) decide the launch plans, and
+// a workspace is sized from those plans: the first answer for a key is kept
+// for the life of the process, so later plans always match the workspace.
+// One table per call site (each passes its own lambda type).
+template <class Query>
+inline int remembered(uint64_t key, Query q) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, int> memo;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+  }
+  const int v = q();
+  std::lock_guard<std::mutex> g(mu);
+  return memo.emplace(key, v).first->second;
+}
+
+inline uint64_t occ_key(int dev, int a, int b, size_t smem) {
+  return ((uint64_t)(dev & 0xFF) << 56) | ((uint64_t)(a & 0xFF) << 48) | ((uint64_t)(b & 0xFF) << 40) |
+         ((uint64_t)smem & 0xFFFFFFFFFFull);
+}
 
 // ----------------------------------------------------------------- layouts --
 // Packed weights: a projection with N output rows and K inputs is cut into

@@ -971,22 +971,27 @@ cudaError_t launch_tc(const ProjArgs& a, int grid, size_t smem, cudaStream_t st,
 }
 
 int resident_tc(int epi, size_t smem) {
-  int dev = 0, n = 0;
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  cudaError_t e = cudaSuccess;
-  if (epi == kEpiResid) {
-    e = configure_tc<kEpiResid>(dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_tc_kernel<kEpiResid>, kTcThreads, smem);
-  } else {
-    e = configure_tc<kEpiSwiglu>(dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_tc_kernel<kEpiSwiglu>, kTcThreads, smem);
-  }
-  return e == cudaSuccess ? n : 0;
+  return remembered(occ_key(dev, 5, epi, smem), [&]() {
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+    if (epi == kEpiResid) {
+      e = configure_tc<kEpiResid>(dev);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_tc_kernel<kEpiResid>, kTcThreads, smem);
+    } else {
+      e = configure_tc<kEpiSwiglu>(dev);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_tc_kernel<kEpiSwiglu>, kTcThreads, smem);
+    }
+    return e == cudaSuccess ? n : 0;
+  });
 }
 
 int resident_ctas(int nt, int epi, size_t smem) {
-  int dev = 0, n = 0;
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return remembered(occ_key(dev, nt, epi, smem), [&]() {
+  int n = 0;
   cudaError_t e = cudaSuccess;
 #define FUTR_OCC(NT_, EPI_)                                                               \
   if (nt == NT_ && epi == EPI_) {                                                         \
@@ -999,6 +1004,7 @@ int resident_ctas(int nt, int epi, size_t smem) {
   FUTR_OCC(1, 2) FUTR_OCC(2, 2) FUTR_OCC(3, 2) FUTR_OCC(4, 2)
 #undef FUTR_OCC
   return e == cudaSuccess ? n : 0;
+  });
 }
 
 }  // namespace
