@@ -178,7 +178,7 @@ def test_decode_toy_workload():
     run_case(wl.shape, wl.batch, inputs.context_lengths(wl), n_outlier=wl.n_outlier)
 
 
-@pytest.mark.parametrize("batch", [1, 2, 3, 7, 8, 9, 16, 31, 32])
+@pytest.mark.parametrize("batch", [1, 2, 3, 7, 8, 9, 16, 17, 24, 31, 32])
 def test_decode_toy_batch_sweep(batch):
     r = np.random.default_rng(batch)
     lengths = r.integers(0, 300, size=batch)
@@ -231,6 +231,30 @@ def test_decode_deterministic_and_splitk_invariant(monkeypatch):
         gpu.append_history(0, hist)
         outs.append(bits_to_f64(gpu.decode(x, pos)))
     np.testing.assert_array_equal(outs[0], outs[1])  # same plan: bit-identical
+    for o in outs[2:]:
+        assert_close(o, outs[0], "split-K", rel=2e-3)
+
+
+def test_decode_batch32_deterministic_and_splitk_invariant(monkeypatch):
+    """Batch 32 runs O and down on the tensor-core kernel: repeated calls are
+    bit-identical and forced splits agree within fp32 reordering."""
+    shape, batch = TOY, 32
+    lengths = [(37 * i) % 211 for i in range(batch)]
+    weights = inputs.block_weights(shape, 9)
+    x = inputs.activations(shape, batch, 9)
+    hist = inputs.kv_history(shape, lengths, seed=9)
+    pos = np.array(lengths, np.int32)
+    outs = []
+    for split in (None, None, "1", "3"):
+        if split is None:
+            monkeypatch.delenv("FUTR_SPLITK", raising=False)
+        else:
+            monkeypatch.setenv("FUTR_SPLITK", split)
+        gpu = GpuBlock(shape, weights, max_batch=batch, capacity=256)
+        gpu.append_history(0, hist)
+        outs.append(bits_to_f64(gpu.decode(x, pos)))
+        assert futr.futr_check(gpu.ws, gpu.kv) == 0
+    np.testing.assert_array_equal(outs[0], outs[1])
     for o in outs[2:]:
         assert_close(o, outs[0], "split-K", rel=2e-3)
 

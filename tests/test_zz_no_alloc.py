@@ -25,7 +25,8 @@ def _case(shape, lengths, seed):
     return gpu, x, pos
 
 
-@pytest.mark.parametrize("shape,lengths", [(TOY, [5, 130, 0]), (LLAMA8B, [1024])], ids=["toy_b3", "8b_b1"])
+@pytest.mark.parametrize("shape,lengths", [(TOY, [5, 130, 0]), (TOY, [(29 * i) % 170 for i in range(32)]),
+                                           (LLAMA8B, [1024])], ids=["toy_b3", "toy_b32", "8b_b1"])
 def test_no_alloc_matches_workspace_entry(shape, lengths):
     gpu, x, pos = _case(shape, lengths, seed=11)
     b = len(lengths)
