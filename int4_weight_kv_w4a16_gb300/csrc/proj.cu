@@ -29,6 +29,9 @@
 //     QKV   : r * acc, RoPE(q, k) at pos, fp32 Hadamard rotation; q -> fp32
 //             rotated query; k, v -> INT4 + fp16 scale into cache slot pos
 //             (direct KV-cache placement, abstract).
+// Batch 17..32 of the residual and SwiGLU projections runs a variant with the
+// same stream, unpacking and epilogue on the 5th-generation tensor cores
+// (tcgen05.mma with A in tensor memory; proj_tc_kernel below).
 #include <cuda.h>
 
 #include "futr_internal.cuh"
