@@ -10,9 +10,12 @@
 //
 // Structure of one CTA (row block of 128 outputs x a K-range of groups):
 //   warp 4 (producer): per 128-input group, one ring stage of shared memory
-//     receives by 1-D bulk copies (mbarrier completion) the weight unit (codes
-//     + scales, 8448 B) and the matching activation tile (one 256-byte row per
-//     batch row, rows padded to 272 B).  Weight units of the first stages are
+//     receives (mbarrier completion) the weight unit (codes + scales, 8448 B)
+//     by a 1-D bulk copy and the matching activation tile by one 2-D tensor
+//     copy: a box of 136 inputs x batch rows lands as rows of 272 bytes (128
+//     inputs + 8 that keep ldmatrix free of bank conflicts; inputs past K read
+//     as zero).  A single row (batch 1) comes by a 256-byte bulk copy, which
+//     measured faster than the tensor copy there.  Weight units of the first stages are
 //     issued before griddepcontrol.wait, so weight streaming overlaps the
 //     previous kernel; activation tiles follow the wait.
 //   warps 0..3 (consumers): warp w owns rows 32w..32w+31 (two 16-row MMA
@@ -139,12 +142,29 @@ __device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, in
     store_v_token<J>(a.kv.stream(n, hg - a.Hq - a.Hkv), a.kv.cap, p, code, s, scratch[warp]);
 }
 
-// Activation tile of group g into a ring stage: one 256-byte bulk copy per
-// batch row, rows kTileLd elements apart.
-__device__ __forceinline__ void issue_tile(const ProjArgs& a, uint8_t* stage, int g, uint64_t* bar) {
-  uint8_t* dst = stage + kUnitBytes;
-  const __nv_bfloat16* src = a.xin + (size_t)g * kGroup;
-  for (int n = 0; n < a.batch; ++n) bulk_g2s(dst + n * (kTileLd * 2), src + (size_t)n * a.K, kGroup * 2, bar);
+__device__ __forceinline__ void tma_2d_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Pull a tensor map (a kernel parameter) into the copy engine's cache ahead of
+// its first use.
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Activation tile of group g into a ring stage: one tensor copy of inputs
+// 128 g .. 128 g + 135 of the batch rows, rows kTileLd elements apart (batch
+// 1: the row's 128 inputs by a bulk copy).
+__device__ __forceinline__ void issue_tile(const ProjArgs& a, const CUtensorMap* xmap, uint8_t* stage, int g,
+                                           uint64_t* bar) {
+  if (a.batch == 1)
+    bulk_g2s(stage + kUnitBytes, a.xin + (size_t)g * kGroup, kGroup * 2, bar);
+  else
+    tma_2d_box(stage + kUnitBytes, xmap, kGroup * g, 0, bar);
 }
 
 // Everything after the K-loop: the epilogue tile (filled by write_red from
@@ -333,8 +353,9 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, uint8_t* smem, int 
 }
 
 template <int NT, int EPI>
-__device__ __forceinline__ void proj_body(const ProjArgs& a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* xmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rb = blockIdx.x / a.S, sk = blockIdx.x - rb * a.S;
   const int g0 = (int)(((long long)sk * a.n_groups) / a.S);
@@ -363,15 +384,16 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a) {
   if (warp == kCW) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
-      const uint32_t tx = kUnitBytes + (uint32_t)a.batch * kGroup * 2;
+      const uint32_t tx = kUnitBytes + (a.batch == 1 ? kGroup * 2 : (uint32_t)a.batch * kTileLd * 2);
       const int pre = ng < R ? ng : R;
+      if (a.batch > 1) prefetch_map(xmap);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], tx);
         bulk_g2s(stages + (size_t)i * a.stage_bytes, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[i]);
       }
       pdl_wait();  // the activations come from the previous kernel
       const unsigned long long deadline = global_ns() + kWaitNs;
-      for (int i = 0; i < pre; ++i) issue_tile(a, stages + (size_t)i * a.stage_bytes, g0 + i, &full[i]);
+      for (int i = 0; i < pre; ++i) issue_tile(a, xmap, stages + (size_t)i * a.stage_bytes, g0 + i, &full[i]);
       int slot = 0;
       uint32_t phase = 0;
       for (int i = R; i < ng; ++i) {
@@ -382,7 +404,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a) {
         uint8_t* st = stages + (size_t)slot * a.stage_bytes;
         mbar_arrive_expect_tx(&full[slot], tx);
         bulk_g2s(st, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[slot]);
-        issue_tile(a, st, g0 + i, &full[slot]);
+        issue_tile(a, xmap, st, g0 + i, &full[slot]);
         if (++slot == R) {
           slot = 0;
           phase ^= 1u;
@@ -609,14 +631,6 @@ __device__ __forceinline__ void tc_ld_row32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
 }
 
-__device__ __forceinline__ void tma_2d_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // activation tile of group g: inputs 128 g .. 128 g + 127 as two 4 KB boxes
 __device__ __forceinline__ void tc_issue_tile(uint8_t* dst, const CUtensorMap* map, int g, uint64_t* bar) {
   tma_2d_box(dst, map, kGroup * g, 0, bar);
@@ -677,6 +691,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (lane == 0) {
       const uint32_t tx = kUnitBytes + kTcTile;
       const int pre = ng < R ? ng : R;
+      prefetch_map(&xmap);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], tx);
         bulk_g2s(stages + (size_t)i * kTcStage + kTcTile, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[i]);
@@ -874,18 +889,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 }
 
 template <int NT, int EPI>
-__global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a) {
-  proj_body<NT, EPI>(a);
+__global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a, const __grid_constant__ CUtensorMap xmap) {
+  proj_body<NT, EPI>(a, &xmap);
 }
 
 // Three or four batch tiles: at most 128 registers, so three CTAs share an SM.
 template <int NT, int EPI>
-__global__ void __maxnreg__(128) proj_kernel_wide(const ProjArgs a) {
-  proj_body<NT, EPI>(a);
+__global__ void __maxnreg__(128) proj_kernel_wide(const ProjArgs a, const __grid_constant__ CUtensorMap xmap) {
+  proj_body<NT, EPI>(a, &xmap);
 }
 
 template <int NT, int EPI>
-constexpr void (*proj_entry())(ProjArgs) {
+constexpr void (*proj_entry())(ProjArgs, CUtensorMap) {
   if constexpr (NT >= 3)
     return proj_kernel_wide<NT, EPI>;
   else
@@ -925,7 +940,9 @@ cudaError_t launch_one(const ProjArgs& a, int grid, size_t smem, cudaStream_t st
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, proj_entry<NT, EPI>(), a);
+  CUtensorMap xmap;
+  if (!make_proj_tile_map(&xmap, a.xin, a.batch, a.K, a.batch)) return cudaErrorInvalidValue;
+  return cudaLaunchKernelEx(&cfg, proj_entry<NT, EPI>(), a, xmap);
 }
 
 template <int EPI>
@@ -1026,10 +1043,12 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   if (p.tc) p.nt = 4;
   // ring stage = weight unit + activation tile; as deep as lets the target
   // number of CTAs share an SM (5 up to batch 8, 3 up to 16, 2 beyond)
-  p.stage_bytes = p.tc ? kTcStage : kUnitBytes + batch * kTileLd * 2;
+  // (mma.sync: rounded to 128 bytes, so every stage and its tile start on a
+  // 128-byte boundary for the tensor copy)
+  p.stage_bytes = p.tc ? kTcStage : (kUnitBytes + batch * kTileLd * 2 + 127) & ~127;
   const int misc = p.tc ? kTcMisc : 32 * 4 + 16 + 2 * kMaxRing * 8;
   const int per_sm = batch <= 8 ? 5 : (p.tc ? 2 : 3);
-  const int budget = 232448 / per_sm - 1024 - misc - 2048 - (p.tc ? 1024 : 0);  // reserve, static arrays, alignment
+  const int budget = 232448 / per_sm - 1024 - misc - 2048 - (p.tc ? 1024 : 128);  // reserve, static arrays, alignment
   int ring = budget / p.stage_bytes;
   if (ring > kMaxRing) ring = kMaxRing;
   if (ring < 2) ring = 2;
@@ -1040,7 +1059,7 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   const int red_bytes = p.nt * 8 * kRedLd * 4 + kCW * 32 * 16 + (epi == kEpiQkv ? batch * 2 * 512 + 256 : 0);
   if (ring_bytes < red_bytes) ring_bytes = red_bytes;
   p.off_misc = (ring_bytes + 127) & ~127;
-  p.smem = (size_t)p.off_misc + misc + (p.tc ? 1024 : 0);  // tc: the base is rounded up to 1024 bytes
+  p.smem = (size_t)p.off_misc + misc + (p.tc ? 1024 : 128);  // the base is rounded up (1024 / 128 bytes)
   // splits: balance waves of resident CTAs; each extra split costs a partial
   // write and a share of the reduction
   const int fit = p.tc ? resident_tc(epi, p.smem) : resident_ctas(p.nt, epi, p.smem);

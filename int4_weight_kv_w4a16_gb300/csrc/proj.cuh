@@ -70,6 +70,7 @@ struct AttnPlan {
 // Tensor map of a tensor-core projection's activation tiles (defined with the
 // other tensor maps in step.cu).
 bool make_act_tile_map(CUtensorMap* m, const void* x, int rows, int K);
+bool make_proj_tile_map(CUtensorMap* m, const void* x, int rows, int K, int box_rows);
 
 AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int force_split);
 cudaError_t launch_attention(const AttnPlan& p, AttnArgs a, int d, cudaStream_t st, bool pdl);

@@ -292,6 +292,22 @@ bool make_act_tile_map(CUtensorMap* m, const void* x, int rows, int K) {
   return make_map(m, x, (uint64_t)K, (uint64_t)rows, 32);
 }
 
+// Activation tiles of an mma.sync projection: boxes of 136 inputs x box_rows
+// rows, no swizzle, landing as rows of 272 bytes (128 inputs + 8 padding
+// elements that the consumer never reads); rows past `rows` and inputs past K
+// read as zero.
+bool make_proj_tile_map(CUtensorMap* m, const void* x, int rows, int K, int box_rows) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {136, (cuuint32_t)box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, elem,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_lm_head(const uint16_t* xg, const uint16_t* w, int vocab, int H, int batch, const float* r,
                            float* logits, int* err, cudaStream_t st, bool pdl) {
   const int nt = (batch + 7) / 8;
