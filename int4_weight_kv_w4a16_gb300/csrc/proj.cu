@@ -37,6 +37,8 @@
 // (tcgen05.mma with A in tensor memory; proj_tc_kernel below).
 #include <cuda.h>
 
+#include <cstring>
+
 #include "futr_internal.cuh"
 #include "proj.cuh"
 
@@ -157,11 +159,12 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 }
 
 // Activation tile of group g into a ring stage: one tensor copy of inputs
-// 128 g .. 128 g + 135 of the batch rows, rows kTileLd elements apart (batch
-// 1: the row's 128 inputs by a bulk copy).
+// 128 g .. 128 g + 135 of the batch rows, rows kTileLd elements apart (one
+// row: its 128 inputs by a bulk copy).
+template <bool kRow1>
 __device__ __forceinline__ void issue_tile(const ProjArgs& a, const CUtensorMap* xmap, uint8_t* stage, int g,
                                            uint64_t* bar) {
-  if (a.batch == 1)
+  if (kRow1)
     bulk_g2s(stage + kUnitBytes, a.xin + (size_t)g * kGroup, kGroup * 2, bar);
   else
     tma_2d_box(stage + kUnitBytes, xmap, kGroup * g, 0, bar);
@@ -352,10 +355,17 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, uint8_t* smem, int 
   }
 }
 
-template <int NT, int EPI>
+// NTP: batch tiles of 8 columns, 1..4; 0 = one batch row (one tile, the
+// activation row by a bulk copy)
+template <int NTP, int EPI>
 __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* xmap) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  constexpr int NT = NTP == 0 ? 1 : NTP;
+  constexpr bool kRow1 = NTP == 0;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  // tensor copies want a 128-byte aligned destination: the base is rounded up
+  // (one row takes only 16-byte aligned bulk copies and uses it as it is)
+  uint8_t* smem = kRow1 ? smem_raw
+                        : reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rb = blockIdx.x / a.S, sk = blockIdx.x - rb * a.S;
   const int g0 = (int)(((long long)sk * a.n_groups) / a.S);
@@ -384,16 +394,16 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
   if (warp == kCW) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
-      const uint32_t tx = kUnitBytes + (a.batch == 1 ? kGroup * 2 : (uint32_t)a.batch * kTileLd * 2);
+      const uint32_t tx = kUnitBytes + (kRow1 ? kGroup * 2 : (uint32_t)a.batch * kTileLd * 2);
       const int pre = ng < R ? ng : R;
-      if (a.batch > 1) prefetch_map(xmap);
+      if (!kRow1) prefetch_map(xmap);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], tx);
         bulk_g2s(stages + (size_t)i * a.stage_bytes, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[i]);
       }
       pdl_wait();  // the activations come from the previous kernel
       const unsigned long long deadline = global_ns() + kWaitNs;
-      for (int i = 0; i < pre; ++i) issue_tile(a, xmap, stages + (size_t)i * a.stage_bytes, g0 + i, &full[i]);
+      for (int i = 0; i < pre; ++i) issue_tile<kRow1>(a, xmap, stages + (size_t)i * a.stage_bytes, g0 + i, &full[i]);
       int slot = 0;
       uint32_t phase = 0;
       for (int i = R; i < ng; ++i) {
@@ -404,7 +414,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
         uint8_t* st = stages + (size_t)slot * a.stage_bytes;
         mbar_arrive_expect_tx(&full[slot], tx);
         bulk_g2s(st, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[slot]);
-        issue_tile(a, xmap, st, g0 + i, &full[slot]);
+        issue_tile<kRow1>(a, xmap, st, g0 + i, &full[slot]);
         if (++slot == R) {
           slot = 0;
           phase ^= 1u;
@@ -941,14 +951,17 @@ cudaError_t launch_one(const ProjArgs& a, int grid, size_t smem, cudaStream_t st
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   CUtensorMap xmap;
-  if (!make_proj_tile_map(&xmap, a.xin, a.batch, a.K, a.batch)) return cudaErrorInvalidValue;
+  if (NT == 0)
+    memset(&xmap, 0, sizeof(xmap));  // one row: no tensor copy
+  else if (!make_proj_tile_map(&xmap, a.xin, a.batch, a.K, a.batch))
+    return cudaErrorInvalidValue;
   return cudaLaunchKernelEx(&cfg, proj_entry<NT, EPI>(), a, xmap);
 }
 
 template <int EPI>
 cudaError_t launch_nt(int nt, const ProjArgs& a, int grid, size_t smem, cudaStream_t st, bool pdl) {
   switch (nt) {
-    case 1: return launch_one<1, EPI>(a, grid, smem, st, pdl);
+    case 1: return a.batch == 1 ? launch_one<0, EPI>(a, grid, smem, st, pdl) : launch_one<1, EPI>(a, grid, smem, st, pdl);
     case 2: return launch_one<2, EPI>(a, grid, smem, st, pdl);
     case 3: return launch_one<3, EPI>(a, grid, smem, st, pdl);
     default: return launch_one<4, EPI>(a, grid, smem, st, pdl);
@@ -1019,9 +1032,9 @@ int resident_ctas(int nt, int epi, size_t smem) {
     if (e == cudaSuccess)                                                                 \
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, proj_entry<NT_, EPI_>(), kThreads, smem); \
   }
-  FUTR_OCC(1, 0) FUTR_OCC(2, 0) FUTR_OCC(3, 0) FUTR_OCC(4, 0)
-  FUTR_OCC(1, 1) FUTR_OCC(2, 1) FUTR_OCC(3, 1) FUTR_OCC(4, 1)
-  FUTR_OCC(1, 2) FUTR_OCC(2, 2) FUTR_OCC(3, 2) FUTR_OCC(4, 2)
+  FUTR_OCC(0, 0) FUTR_OCC(1, 0) FUTR_OCC(2, 0) FUTR_OCC(3, 0) FUTR_OCC(4, 0)
+  FUTR_OCC(0, 1) FUTR_OCC(1, 1) FUTR_OCC(2, 1) FUTR_OCC(3, 1) FUTR_OCC(4, 1)
+  FUTR_OCC(0, 2) FUTR_OCC(1, 2) FUTR_OCC(2, 2) FUTR_OCC(3, 2) FUTR_OCC(4, 2)
 #undef FUTR_OCC
   return e == cudaSuccess ? n : 0;
   });
@@ -1062,7 +1075,7 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   p.smem = (size_t)p.off_misc + misc + (p.tc ? 1024 : 128);  // the base is rounded up (1024 / 128 bytes)
   // splits: balance waves of resident CTAs; each extra split costs a partial
   // write and a share of the reduction
-  const int fit = p.tc ? resident_tc(epi, p.smem) : resident_ctas(p.nt, epi, p.smem);
+  const int fit = p.tc ? resident_tc(epi, p.smem) : resident_ctas(batch == 1 ? 0 : p.nt, epi, p.smem);
   const long long slots = (long long)n_sm * (fit > 0 ? fit : 1);
   int best_s = 1;
   double best = 1e30;
