@@ -27,11 +27,15 @@ ERRORS = []
 
 
 def record_errors(shape, batch, errs):
+    """Keep the measured errors; with FUTR_PARITY_LOG set, also append them
+    to that file (one JSON line per case)."""
     ERRORS.append({"hidden": shape.hidden, "batch": batch, **errs})
     import json, os
-    os.makedirs("gpurun_out", exist_ok=True)
-    with open("gpurun_out/parity_errors.jsonl", "a") as f:
-        f.write(json.dumps(ERRORS[-1]) + "\n")
+    path = os.environ.get("FUTR_PARITY_LOG")
+    if path:
+        os.makedirs(os.path.dirname(path) or ".", exist_ok=True)
+        with open(path, "a") as f:
+            f.write(json.dumps(ERRORS[-1]) + "\n")
 
 
 PROJ = {"qkv": futr.FUTR_PROJ_QKV, "o": futr.FUTR_PROJ_O, "gate": futr.FUTR_PROJ_GATE,
