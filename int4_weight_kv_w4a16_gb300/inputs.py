@@ -74,6 +74,7 @@ LLAMA70B = BlockShape(hidden=8192, n_q_heads=64, n_kv_heads=8, head_dim=128, int
 WORKLOADS: Dict[str, Workload] = {
     "toy_b1_ctx128": Workload("toy_b1_ctx128", TOY, 1, 128, n_outlier=4),
     "llama8b_b1_ctx1024": Workload("llama8b_b1_ctx1024", LLAMA8B, 1, 1024),
+    "llama8b_b8_ctx1024": Workload("llama8b_b8_ctx1024", LLAMA8B, 8, 1024),
     "llama8b_b32_ragged512-4096": Workload("llama8b_b32_ragged512-4096", LLAMA8B, 32, 4096,
                                            ragged=(512, 4096)),
     "llama70b_b1_ctx2048": Workload("llama70b_b1_ctx2048", LLAMA70B, 1, 2048),

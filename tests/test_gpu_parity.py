@@ -213,6 +213,11 @@ def test_decode_8b_b1_ctx1024():
     run_case(wl.shape, wl.batch, inputs.context_lengths(wl))
 
 
+def test_decode_8b_b8_ctx1024():
+    wl = WORKLOADS["llama8b_b8_ctx1024"]
+    run_case(wl.shape, wl.batch, inputs.context_lengths(wl))
+
+
 def test_decode_8b_b32_ragged():
     wl = WORKLOADS["llama8b_b32_ragged512-4096"]
     run_case(wl.shape, wl.batch, inputs.context_lengths(wl), check_codes=True)
