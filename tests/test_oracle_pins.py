@@ -177,6 +177,71 @@ def test_quant_weight_group_layout():
     assert others.max() < 0.02
 
 
+# ------------------------------------------------ dequantization and cache --
+
+def test_dequant_hand_case():
+    # two rows of four codes in groups of two: each value is its code times the
+    # scale of its own (row, group)
+    codes = np.array([[1, -8, 7, 0], [3, 3, -1, 2]], np.int8)
+    scales = np.array([[0.5, 2.0], [0.25, 4.0]], np.float16)
+    np.testing.assert_array_equal(oracle.dequant(codes, scales, 2),
+                                  [[0.5, -4.0, 14.0, 0.0], [0.75, 0.75, -4.0, 8.0]])
+
+
+def test_dequant_block_roundtrip_within_half_scale():
+    """|dequant(pack(W)) - W diag(g)| <= s/2 with s = fp16(absmax/7) of the
+    element's own (row, 128-input group).  The magnitudes differ by powers of
+    ten between neighbouring rows and groups, so a scale applied to another
+    row or group, or a gain folded into the wrong projection, breaks the bound
+    by orders of magnitude.  The bound is taken from the group's absmax, not
+    from the packed scales."""
+    sh = oracle_shape_tiny(hidden=256, inter=256, head_dim=32, had_block=32, group=128)
+    r = np.random.default_rng(18)
+
+    def mk(o, i):
+        mag = 10.0 ** (np.arange(o)[:, None] % 3 + 2 * (np.arange(i)[None, :] // 128) - 2)
+        return (r.standard_normal((o, i)) * mag).astype(np.float32)
+
+    w = {"wq": mk(sh.q_rows, 256), "wk": mk(sh.kv_rows, 256), "wv": mk(sh.kv_rows, 256),
+         "wo": mk(256, sh.q_rows), "wgate": mk(256, 256), "wup": mk(256, 256), "wdown": mk(256, 256),
+         "g_attn": r.uniform(0.5, 1.5, 256).astype(np.float32),
+         "g_mlp": r.uniform(0.5, 1.5, 256).astype(np.float32)}
+    f64 = lambda a: np.asarray(a, np.float64)
+    target = {"qkv": np.concatenate([w["wq"], w["wk"], w["wv"]]) * f64(w["g_attn"]),
+              "o": f64(w["wo"]), "gate": w["wgate"] * f64(w["g_mlp"]), "up": w["wup"] * f64(w["g_mlp"]),
+              "down": f64(w["wdown"])}
+    dq = oracle.dequant_block(oracle.pack_block(w))
+    for k, t in target.items():
+        n, kk = t.shape
+        amax = np.abs(t.reshape(n, kk // 128, 128)).max(-1)
+        half_s = np.repeat(amax / 14.0 * (1 + 2.0 ** -10), 128, axis=1)
+        assert dq[k].shape == t.shape
+        assert np.all(np.abs(dq[k] - t) <= half_s + 1e-6 * np.abs(t)), k
+
+
+def test_build_cache_matches_bruteforce():
+    # every cached token and kv-head: fp32 butterflies of the bf16 history
+    # vector, then the quantizer, both by the pure-Python brute force
+    sh = oracle_shape_tiny()
+    r = np.random.default_rng(19)
+    hist = []
+    for L in (3, 0, 2):
+        k = r.standard_normal((sh.n_kv_heads, L, sh.head_dim))
+        k[..., 1] *= 20
+        hist.append((_bf16_bits(k), _bf16_bits(r.standard_normal((sh.n_kv_heads, L, sh.head_dim)))))
+    cache = oracle.build_cache(hist, sh)
+    assert len(cache) == len(hist)
+    for (kb, vb), c in zip(hist, cache):
+        for name, bits in (("k", kb), ("v", vb)):
+            vals = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+            assert c[name + "_codes"].shape == bits.shape
+            for h in range(sh.n_kv_heads):
+                for t in range(bits.shape[1]):
+                    codes, s = bf.quant(bf.fwht_f32(list(vals[h, t]), sh.had_block))
+                    assert float(c[name + "_scales"][h, t]) == s
+                    np.testing.assert_array_equal(c[name + "_codes"][h, t], codes)
+
+
 # ------------------------------------------------------------ gain folding --
 
 def test_gain_folding_equals_rmsnorm_then_matmul():
@@ -385,17 +450,21 @@ def test_final_logits_gain_rounded_once_to_bf16():
 
 
 def test_final_logits_reads_rows_of_the_head():
-    # one-hot rows: logit v is r * bf16(g_v y_v); a transposed head or a dropped
-    # factor fails
+    # one-hot rows: logit v is r * bf16(fp32(g_k y_k)) for the column k the row
+    # selects; the gain differs per column and g_k y_k is not a bf16 value, so
+    # a transposed head, a gain of another column, a dropped factor or an
+    # activation left unrounded fails.  Rounding by the brute-force helpers.
     H = 16
     y = oracle.bf16_bits_to_float(_bf16_bits(np.arange(1, H + 1, dtype=np.float32) / 4))[None, :]
     w = np.zeros((6, H), np.float32)
     for v in range(6):
         w[v, 3 * v % H] = 1.0
-    g = np.full(H, 2.0, np.float32)
+    g = (1.0 + np.arange(H, dtype=np.float32) / np.float32(10.0)).astype(np.float32)
     got = oracle.final_logits(y, g, _bf16_bits(w), 1e-5)[0]
-    r = 1.0 / math.sqrt(float(np.mean(y * y)) + 1e-5)
-    np.testing.assert_allclose(got, [r * 2.0 * y[0, 3 * v % H] for v in range(6)], rtol=1e-15)
+    r = 1.0 / math.sqrt(sum(float(a) ** 2 for a in y[0]) / H + 1e-5)
+    act = [bf.bf16(bf.f32(float(g[k]) * float(y[0, k]))) for k in range(H)]
+    assert sum(act[k] != float(g[k]) * float(y[0, k]) for k in range(H)) >= 8  # the rounding matters
+    np.testing.assert_allclose(got, [r * act[3 * v % H] for v in range(6)], rtol=1e-15)
 
 
 def test_decode_step_chains_the_blocks():
