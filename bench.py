@@ -178,6 +178,26 @@ def barrier(world: int):
 
 # ----------------------------------------------------------- CPU baseline --
 
+def host_info() -> dict:
+    """CPU model, BLAS library and BLAS thread setting of the host that times the oracle."""
+    import platform
+    import subprocess
+    model = platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        names = [ln.split(":", 1)[1].strip() for ln in out.splitlines() if ln.startswith("Model name:")]
+        if names:
+            model = f"{names[0]} ({platform.machine()})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        blas = np.show_config(mode="dicts")["Build Dependencies"]["blas"]["name"]
+    except Exception:  # older numpy: no dict form of the build configuration
+        blas = "unknown"
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or "library default"
+    return {"cpu_model": model, "blas": blas, "blas_threads": threads}
+
+
 def oracle_baseline(wl, budget_s: float = 15.0, max_steps: int = 20, min_steps: int = 1):
     """Time the float64 oracle's decode_block on the host cores, on the same
     workload, for a bounded number of block-steps."""
@@ -201,7 +221,7 @@ def oracle_baseline(wl, budget_s: float = 15.0, max_steps: int = 20, min_steps: 
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": 1e6 * statistics.mean(times), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(times)} full block-steps of {wl.name} (float64 numpy, weights pre-dequantized "
-                      f"outside the timed region)"}
+                      f"outside the timed region)", **host_info()}
 
 
 # ------------------------------------------------------------- GPU bench --
@@ -500,7 +520,8 @@ def step_oracle_baseline(wl, budget_rows: int = 8192):
     us = 1e6 * (t_block * wl.n_layers + t_head)
     return {"value": round(us, 1), "unit": STEP_UNIT, "cores": cores, "kind": "oracle",
             "sample": f"1 block-step of {sh.hidden}-hidden batch {wl.batch} x {wl.n_layers} layers + final norm and "
-                      f"LM head on {budget_rows} of {wl.vocab} rows scaled to the vocabulary (float64 numpy)"}
+                      f"LM head on {budget_rows} of {wl.vocab} rows scaled to the vocabulary (float64 numpy)",
+            **host_info()}
 
 
 def run_step(args, wl):
@@ -587,7 +608,8 @@ def run_reference(args, wl):
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "batch": wl.batch},
             "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{args.steps} full block-steps of {wl.name}, float64 numpy oracle"},
+                             "sample": f"{args.steps} full block-steps of {wl.name}, float64 numpy oracle",
+                             **host_info()},
             "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

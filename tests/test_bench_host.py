@@ -91,3 +91,12 @@ def test_clock_sampler_without_nvidia_smi():
     s = object.__new__(bench.ClockSampler)
     s.p = None
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_cpu_baseline_names_the_host():
+    from int4_weight_kv_w4a16_gb300.inputs import WORKLOADS
+    info = bench.host_info()
+    assert set(info) == {"cpu_model", "blas", "blas_threads"} and all(isinstance(v, str) and v for v in info.values())
+    base = bench.oracle_baseline(WORKLOADS["toy_b1_ctx128"], budget_s=0.5, max_steps=3)
+    assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] > 0
+    assert base["cpu_model"] == info["cpu_model"] and "block-steps of toy_b1_ctx128" in base["sample"]
