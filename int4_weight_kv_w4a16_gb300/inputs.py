@@ -22,7 +22,7 @@ import numpy as np
 # component -> spawn key (fixed; changing one changes every seeded input)
 _STREAM = {
     "wq": 1, "wk": 2, "wv": 3, "wo": 4, "wgate": 5, "wup": 6, "wdown": 7,
-    "g_attn": 8, "g_mlp": 9, "x": 10, "lengths": 11, "outliers": 12, "kv": 13,
+    "g_attn": 8, "g_mlp": 9, "x": 10, "lengths": 11, "outliers": 12, "kv": 13, "calib": 14,
 }
 
 
@@ -164,6 +164,20 @@ def kv_history(shape: BlockShape, lengths: Sequence[int], n_outlier: int = 4,
             k[h][:, chans[h]] *= np.float32(gain)
         out.append((to_bf16_bits(k), to_bf16_bits(v)))
     return out
+
+
+def calibration_inputs(k: int, n: int, seed: int = 0, rank: int = 8, spread: float = 4.0) -> np.ndarray:
+    """Synthetic calibration inputs of one projection, fp32 [n, k]: a rank-`rank`
+    shared part plus independent noise, each channel then scaled by a factor
+    drawn log-uniformly from [1/spread, spread].  The channels are correlated and
+    unevenly scaled, as the inputs of a trained model's projections are; there
+    is no trained model here to take them from."""
+    r = rng_for(seed, "calib")
+    z = r.standard_normal((n, rank), dtype=np.float32)
+    mix = r.standard_normal((rank, k), dtype=np.float32)
+    noise = r.standard_normal((n, k), dtype=np.float32)
+    scale = np.exp(r.uniform(-np.log(spread), np.log(spread), k)).astype(np.float32)
+    return ((z @ mix + noise) * scale).astype(np.float32)
 
 
 # Device-side generators for the complete-model workloads (32 layers of fp32

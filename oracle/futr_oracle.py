@@ -39,6 +39,14 @@ Readings of points the pages leave open (the plainest one each time):
     cannot be folded into INT4 codes).  The final gain multiplies the last
     block's output in fp32 and the product is rounded once to bf16, the LM
     head's activation; the RMSNorm factor r (float64 here) scales the logits.
+  * GPTQ "in the same format": the same INT4 codes and one fp16 scale per
+    (output row, 128 inputs), chosen by the published GPTQ column sweep
+    (natural column order, 1 % dampening, upper Cholesky factor of the inverse
+    Hessian).  Each group's scale follows the rule of the round-to-nearest
+    quantizer, applied to the group's error-compensated weights when the sweep
+    reaches the group's first column.  The Hessian is that of the normalized
+    input the gain-folded weight multiplies.  The sweep's working weights are
+    float64; every code and scale decision is taken on their fp32 rounding.
 """
 from __future__ import annotations
 
@@ -130,23 +138,33 @@ def fwht_f32(v: np.ndarray, n: int) -> np.ndarray:
 FP16_MAX = 65504.0
 
 
-def quant_rtn(v32: np.ndarray):
-    """Quantize each vector along the last axis to signed INT4 with one fp16 scale.
-
-    a = max |v| (exact), s = fp16(a / 7) with the division in fp32 (a quotient
-    above the fp16 range saturates to 65504), code = clamp(rint(v / s), -8, 7)
-    with v / s an fp32 division and rint ties-to-even.  s == 0 gives all-zero
-    codes.  Returns (codes int8, scales float16).
-    """
+def rtn_scale(v32: np.ndarray) -> np.ndarray:
+    """The scale of each vector along the last axis: a = max |v| (exact),
+    s = fp16(a / 7) with the division in fp32 (a quotient above the fp16 range
+    saturates to 65504).  Returns float16 [...]."""
     v = np.asarray(v32, dtype=np.float32)
     a = np.max(np.abs(v), axis=-1)
     q7 = (a / np.float32(7.0)).astype(np.float32)
-    s16 = np.minimum(q7, np.float32(FP16_MAX)).astype(np.float16)
-    s32 = s16.astype(np.float32)[..., None]
+    return np.minimum(q7, np.float32(FP16_MAX)).astype(np.float16)
+
+
+def rtn_codes(v32: np.ndarray, s16: np.ndarray) -> np.ndarray:
+    """Codes of each vector along the last axis under its scale s:
+    clamp(rint(v / s), -8, 7) with v / s an fp32 division and rint
+    ties-to-even; s == 0 gives all-zero codes.  Returns int8 [..., n]."""
+    v = np.asarray(v32, dtype=np.float32)
+    s32 = np.asarray(s16, dtype=np.float16).astype(np.float32)[..., None]
     safe = np.where(s32 > 0, s32, np.float32(1.0))
     q = (v / safe).astype(np.float32)
-    c = np.where(s32 > 0, np.clip(np.rint(q), -8, 7), 0).astype(np.int8)
-    return c, s16
+    return np.where(s32 > 0, np.clip(np.rint(q), -8, 7), 0).astype(np.int8)
+
+
+def quant_rtn(v32: np.ndarray):
+    """Quantize each vector along the last axis to signed INT4 with one fp16
+    scale: s = ``rtn_scale(v)``, codes = ``rtn_codes(v, s)``.  Returns
+    (codes int8, scales float16)."""
+    s16 = rtn_scale(v32)
+    return rtn_codes(v32, s16), s16
 
 
 def dequant(codes: np.ndarray, scales: np.ndarray, group: int) -> np.ndarray:
@@ -201,6 +219,84 @@ def pack_block(weights: Dict[str, np.ndarray], group: int = 128) -> Dict[str, tu
 
 def dequant_block(packed: Dict[str, tuple], group: int = 128) -> Dict[str, np.ndarray]:
     return {k: dequant(c, s, group) for k, (c, s) in packed.items()}
+
+
+# ----------------------------------------------------------------------------
+# GPTQ in the same INT4 format  [ABS] "GPTQ in the same format"; the explainer's
+# paragraph on GPTQ (calibration data, approximate second-order information).
+# The pages name the method only; its steps here are those of the published
+# GPTQ algorithm (Frantar et al., "GPTQ: Accurate Post-Training Quantization
+# for Generative Pre-trained Transformers", 2022), without activation reordering.
+# ----------------------------------------------------------------------------
+
+
+def gptq_hessian(xcal: np.ndarray) -> np.ndarray:
+    """H = (2/n) X^T X for n calibration inputs X [n, K] (float64): the Hessian,
+    with respect to each row of the quantized weight, of the mean squared
+    output error (1/n) sum_i ||(W - Q) x_i||^2."""
+    x = np.asarray(xcal, dtype=np.float64)
+    return (2.0 / x.shape[0]) * (x.T @ x)
+
+
+def gptq_quantize(w32: np.ndarray, h: np.ndarray, group: int = 128, damp: float = 0.01):
+    """Quantize W [N, K] (fp32) to the format of ``quantize_weight``, choosing
+    the codes by GPTQ under the input Hessian h [K, K].
+
+    1. An input that is zero in all calibration data (H_jj = 0) gets H_jj = 1,
+       and its weight column is set to 0.
+    2. Dampening: H += damp * mean(diag H) * I.
+    3. U = the upper Cholesky factor of H^-1 (H^-1 = U^T U).
+    4. Columns j = 0 .. K-1 in order, on a float64 working copy of W:
+       at the first column of each group of `group` inputs the group's scales
+       are ``rtn_scale`` of the group's current weights (in fp32);
+       column j's codes are ``rtn_codes`` of its current weights (in fp32)
+       under those scales; its error e = (w_j - c_j s) / U_jj is spread over
+       the columns not yet quantized, W[:, j+1:] -= e U[j, j+1:].
+    With a diagonal H no error is spread and the result is the round-to-nearest
+    quantizer's.  Returns codes int8 [N, K] and fp16 scales [N, K/group]."""
+    w = np.array(w32, dtype=np.float32).astype(np.float64)
+    n, k = w.shape
+    assert k % group == 0 and h.shape == (k, k)
+    hh = np.array(h, dtype=np.float64, copy=True)
+    dead = np.diag(hh) == 0
+    hh[dead, dead] = 1.0
+    w[:, dead] = 0.0
+    hh[np.diag_indices(k)] += damp * np.mean(np.diag(hh))
+    u = np.linalg.cholesky(np.linalg.inv(hh)).T
+    codes = np.zeros((n, k), dtype=np.int8)
+    scales = np.zeros((n, k // group), dtype=np.float16)
+    for j in range(k):
+        gi = j // group
+        if j % group == 0:
+            scales[:, gi] = rtn_scale(w[:, j:j + group].astype(np.float32))
+        c = rtn_codes(w[:, j:j + 1].astype(np.float32), scales[:, gi])[:, 0]
+        codes[:, j] = c
+        e = (w[:, j] - c * scales[:, gi].astype(np.float64)) / u[j, j]
+        w[:, j + 1:] -= np.outer(e, u[j, j + 1:])
+    return codes, scales
+
+
+def gptq_quantize_weight(w: np.ndarray, g: Optional[np.ndarray], h: np.ndarray, group: int = 128,
+                         damp: float = 0.01):
+    """Fold the gain (W' = W diag(g), one fp32 rounding), then ``gptq_quantize``
+    with the Hessian of the normalized input the folded weight multiplies."""
+    return gptq_quantize(fold_gain(w, g), h, group, damp)
+
+
+def pack_block_gptq(weights: Dict[str, np.ndarray], hessians: Dict[str, np.ndarray], group: int = 128,
+                    damp: float = 0.01) -> Dict[str, tuple]:
+    """``pack_block`` with GPTQ codes.  hessians: 'attn' [H, H] of the normalized
+    block input (QKV), 'o' [Hq*d, Hq*d] of the attention output, 'mlp' [H, H] of
+    the normalized residual (gate and up), 'down' [I, I] of the SwiGLU output."""
+    ga, gm = weights["g_attn"], weights["g_mlp"]
+    wqkv = np.concatenate([weights["wq"], weights["wk"], weights["wv"]], axis=0)
+    return {
+        "qkv": gptq_quantize_weight(wqkv, ga, hessians["attn"], group, damp),
+        "o": gptq_quantize_weight(weights["wo"], None, hessians["o"], group, damp),
+        "gate": gptq_quantize_weight(weights["wgate"], gm, hessians["mlp"], group, damp),
+        "up": gptq_quantize_weight(weights["wup"], gm, hessians["mlp"], group, damp),
+        "down": gptq_quantize_weight(weights["wdown"], None, hessians["down"], group, damp),
+    }
 
 
 # ----------------------------------------------------------------------------

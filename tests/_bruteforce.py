@@ -128,3 +128,46 @@ def block(x, w, cache, pos, sh):
     act = [bf16(gg / (1.0 + math.exp(-gg)) * uu) for gg, uu in zip(g, u)]
     y = [bf16(a + b) for a, b in zip(hres, matvec(w["down"], act))]
     return {"q_rot": q_rot, "k_new": k_new, "v_new": v_new, "o": o, "h": hres, "a": act, "y": y}
+
+
+def code(x: float, s: float) -> int:
+    """The INT4 code of x under scale s (0 when s == 0)."""
+    if s == 0:
+        return 0
+    return max(-8, min(7, round(f32(f32(x) / s))))
+
+
+def gptq_row(w, h, group, damp):
+    """GPTQ of one weight row by its least-squares definition: after columns
+    0..j-1 are fixed to their quantized values, the remaining weights are the
+    minimizers of (w - v) H (w - v)^T over v with the fixed part held, i.e.
+    v_R = w_R + H_RR^-1 H_RF (w_F - q_F), solved afresh at every column; column
+    j is then quantized from v_j.  Same dead-input and dampening rules as the
+    published algorithm.  numpy is used for the linear solves only."""
+    import numpy as np
+    k = len(w)
+    hh = np.array(h, dtype=np.float64, copy=True)
+    w = np.array([f32(a) for a in w], dtype=np.float64)
+    for j in range(k):
+        if hh[j, j] == 0:
+            hh[j, j] = 1.0
+            w[j] = 0.0
+    mean_diag = sum(hh[j, j] for j in range(k)) / k
+    for j in range(k):
+        hh[j, j] += damp * mean_diag
+    q = []
+    codes, scales = [], []
+    s = 0.0
+    for j in range(k):
+        fixed, rest = list(range(j)), list(range(j, k))
+        v = w[rest].copy()
+        if fixed:
+            delta = w[fixed] - np.array(q)
+            v += np.linalg.solve(hh[np.ix_(rest, rest)], hh[np.ix_(rest, fixed)] @ delta)
+        if j % group == 0:
+            s = quant(list(v[:group]))[1]
+            scales.append(s)
+        c = code(float(v[0]), s)
+        codes.append(c)
+        q.append(c * s)
+    return codes, scales

@@ -24,7 +24,7 @@ ORIG = {name: getattr(O, name) for name in (
     "rope", "stage_attention", "fwht_f32", "hadamard", "rotate", "quant_rtn", "dequant", "fold_gain",
     "pack_block", "rms_factor", "stage_qkv", "stage_o", "stage_mlp_in", "stage_down", "silu", "final_logits",
     "embed", "decode_step", "round_bf16", "online_softmax_attention", "softmax_attention", "build_cache",
-    "new_kv_codes")}
+    "new_kv_codes", "gptq_quantize", "gptq_hessian", "pack_block_gptq")}
 
 
 def _pins():
@@ -38,8 +38,9 @@ def _pins():
             out.append((name, fn, {}))
             continue
         assert len(marks) == 1
-        arg, values = marks[0].args[0], marks[0].args[1]
-        out.extend((f"{name}[{i}]", fn, {arg: v}) for i, v in enumerate(values))
+        names = [a.strip() for a in marks[0].args[0].split(",")]
+        for i, v in enumerate(marks[0].args[1]):
+            out.append((f"{name}[{i}]", fn, dict(zip(names, v)) if len(names) > 1 else {names[0]: v}))
     return out
 
 
@@ -319,6 +320,52 @@ def _new_kv(rotate=True):
     return new_kv_codes
 
 
+def _gptq(divide=True, spread_sign=1.0, scale_from_current=True, dampen=True, zero_dead=True, upper=True):
+    def gptq_quantize(w32, h, group=128, damp=0.01):
+        w = np.array(w32, dtype=np.float32).astype(np.float64)
+        n, k = w.shape
+        hh = np.array(h, dtype=np.float64, copy=True)
+        dead = np.diag(hh) == 0
+        hh[dead, dead] = 1.0
+        if zero_dead:
+            w[:, dead] = 0.0
+        w0 = w.copy()
+        if dampen:
+            hh[np.diag_indices(k)] += damp * np.mean(np.diag(hh))
+        low = np.linalg.cholesky(np.linalg.inv(hh))
+        u = low.T if upper else low
+        codes = np.zeros((n, k), dtype=np.int8)
+        scales = np.zeros((n, k // group), dtype=np.float16)
+        for j in range(k):
+            gi = j // group
+            if j % group == 0:
+                src = w if scale_from_current else w0
+                scales[:, gi] = O.rtn_scale(src[:, j:j + group].astype(np.float32))
+            c = O.rtn_codes(w[:, j:j + 1].astype(np.float32), scales[:, gi])[:, 0]
+            codes[:, j] = c
+            e = (w[:, j] - c * scales[:, gi].astype(np.float64)) / (u[j, j] if divide else 1.0)
+            w[:, j + 1:] -= spread_sign * np.outer(e, u[j, j + 1:])
+        return codes, scales
+    return gptq_quantize
+
+
+def _hessian(factor=2.0):
+    def gptq_hessian(xcal):
+        x = np.asarray(xcal, dtype=np.float64)
+        return (factor / x.shape[0]) * (x.T @ x)
+    return gptq_hessian
+
+
+def _pack_gptq(down_key="down", o_key="o"):
+    def pack_block_gptq(weights, hessians, group=128, damp=0.01):
+        wqkv = np.concatenate([weights["wq"], weights["wk"], weights["wv"]], axis=0)
+        q = lambda m, g, hk: O.gptq_quantize_weight(m, g, hessians[hk], group, damp)
+        return {"qkv": q(wqkv, weights["g_attn"], "attn"), "o": q(weights["wo"], None, o_key),
+                "gate": q(weights["wgate"], weights["g_mlp"], "mlp"), "up": q(weights["wup"], weights["g_mlp"], "mlp"),
+                "down": q(weights["wdown"], None, down_key)}
+    return pack_block_gptq
+
+
 # (oracle function, factory, mistake-free arguments, planted mistake)
 CASES = {
     "rope_reversed_rotation": ("rope", _rope, {}, dict(sign=-1.0)),
@@ -363,6 +410,14 @@ CASES = {
     "cache_k_v_swapped": ("build_cache", _build_cache, {}, dict(swap_kv=True)),
     "cache_not_rotated": ("build_cache", _build_cache, {}, dict(rotate=False)),
     "new_token_not_rotated": ("new_kv_codes", _new_kv, {}, dict(rotate=False)),
+    "gptq_error_not_divided": ("gptq_quantize", _gptq, {}, dict(divide=False)),
+    "gptq_error_spread_sign": ("gptq_quantize", _gptq, {}, dict(spread_sign=-1.0)),
+    "gptq_scale_from_original_weights": ("gptq_quantize", _gptq, {}, dict(scale_from_current=False)),
+    "gptq_undampened": ("gptq_quantize", _gptq, {}, dict(dampen=False)),
+    "gptq_dead_inputs_kept": ("gptq_quantize", _gptq, {}, dict(zero_dead=False)),
+    "gptq_lower_cholesky_factor": ("gptq_quantize", _gptq, {}, dict(upper=False)),
+    "gptq_hessian_unscaled": ("gptq_hessian", _hessian, {}, dict(factor=1.0)),
+    "gptq_down_with_mlp_hessian": ("pack_block_gptq", _pack_gptq, {}, dict(down_key="mlp")),
 }
 
 

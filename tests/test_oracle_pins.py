@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+from int4_weight_kv_w4a16_gb300 import inputs
 from tests import _bruteforce as bf
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -240,6 +241,87 @@ def test_build_cache_matches_bruteforce():
                     codes, s = bf.quant(bf.fwht_f32(list(vals[h, t]), sh.had_block))
                     assert float(c[name + "_scales"][h, t]) == s
                     np.testing.assert_array_equal(c[name + "_codes"][h, t], codes)
+
+
+# -------------------------------------------------------------------- GPTQ --
+
+def test_gptq_hessian_quadratic_form():
+    # u^T H u is the mean squared output of the linear map u over the
+    # calibration inputs, times 2
+    x = inputs.calibration_inputs(24, 50, seed=20).astype(np.float64)
+    h = oracle.gptq_hessian(x)
+    for u in np.random.default_rng(21).standard_normal((5, 24)):
+        ref = 2.0 / 50 * sum(float(xi @ u) ** 2 for xi in x)
+        assert abs(float(u @ h @ u) - ref) <= 1e-12 * ref
+    np.testing.assert_array_equal(h, h.T)
+
+
+def test_gptq_diagonal_hessian_is_round_to_nearest():
+    # uncorrelated inputs: no error is spread, every (row, group) is the
+    # round-to-nearest quantizer of its own weights
+    r = np.random.default_rng(22)
+    w = (r.standard_normal((8, 256)) * 0.02).astype(np.float32)
+    h = np.diag(r.uniform(0.1, 10.0, 256))
+    c, s = oracle.gptq_quantize(w, h, 128)
+    for i in range(8):
+        for g in range(2):
+            rc, rs = bf.quant([float(a) for a in w[i, 128 * g:128 * (g + 1)]])
+            assert float(s[i, g]) == rs
+            np.testing.assert_array_equal(c[i, 128 * g:128 * (g + 1)], rc)
+
+
+@pytest.mark.parametrize("k,group", [(24, 8), (16, 16)])
+def test_gptq_matches_least_squares_definition(k, group):
+    """The sweep's codes and scales equal those of the definition: after each
+    column is fixed, re-solve the least-squares problem for the columns not yet
+    quantized (pure Python with numpy linear solves, no Cholesky factor).  One
+    input channel is zero in all calibration data."""
+    x = inputs.calibration_inputs(k, 200, seed=23 + k).astype(np.float64)
+    x[:, 5] = 0.0
+    h = oracle.gptq_hessian(x)
+    w = (np.random.default_rng(24).standard_normal((4, k)) * 0.5).astype(np.float32)
+    c, s = oracle.gptq_quantize(w, h, group)
+    assert np.all(c[:, 5] == 0)
+    for i in range(4):
+        rc, rs = bf.gptq_row([float(a) for a in w[i]], h, group, 0.01)
+        np.testing.assert_array_equal(c[i], rc)
+        assert [float(a) for a in s[i]] == rs
+    # with correlated inputs the sweep departs from round-to-nearest
+    assert np.any(c != oracle.quantize_weight(w, None, group)[0])
+
+
+def test_gptq_lowers_calibration_output_error():
+    # the method's purpose: a smaller output error on the calibration inputs
+    # (and on fresh inputs of the same distribution) than round-to-nearest
+    k, n = 256, 1024
+    xs = inputs.calibration_inputs(k, 2 * n, seed=25).astype(np.float64)
+    x, held_out = xs[:n], xs[n:]
+    w = (np.random.default_rng(26).standard_normal((64, k)) * 0.02).astype(np.float32)
+    err = lambda q, xx: float(np.mean(np.sum(((q - w.astype(np.float64)) @ xx.T) ** 2, axis=0)))
+    q_gptq = oracle.dequant(*oracle.gptq_quantize(w, oracle.gptq_hessian(x), 128), 128)
+    q_rtn = oracle.dequant(*oracle.quantize_weight(w, None, 128), 128)
+    assert err(q_gptq, x) < 0.7 * err(q_rtn, x)
+    assert err(q_gptq, held_out) < 0.8 * err(q_rtn, held_out)
+
+
+def test_pack_block_gptq_uses_each_projection_hessian():
+    sh = oracle_shape_tiny(hidden=128, inter=128, head_dim=32, had_block=32, group=128)
+    r = np.random.default_rng(28)
+    mk = lambda o, i: (r.standard_normal((o, i)) * 0.02).astype(np.float32)
+    w = {"wq": mk(sh.q_rows, 128), "wk": mk(sh.kv_rows, 128), "wv": mk(sh.kv_rows, 128),
+         "wo": mk(128, sh.q_rows), "wgate": mk(128, 128), "wup": mk(128, 128), "wdown": mk(128, 128),
+         "g_attn": r.uniform(0.5, 1.5, 128).astype(np.float32), "g_mlp": r.uniform(0.5, 1.5, 128).astype(np.float32)}
+    diag = {k: np.diag(r.uniform(0.5, 2.0, 128)) for k in ("attn", "o", "mlp", "down")}
+    rtn = oracle.pack_block(w)
+    base = oracle.pack_block_gptq(w, diag)
+    for k in rtn:  # diagonal Hessians: the round-to-nearest packer, gains included
+        np.testing.assert_array_equal(base[k][0], rtn[k][0])
+        np.testing.assert_array_equal(base[k][1], rtn[k][1])
+    corr = oracle.gptq_hessian(inputs.calibration_inputs(128, 400, seed=29).astype(np.float64))
+    for hk, changed in (("attn", {"qkv"}), ("o", {"o"}), ("mlp", {"gate", "up"}), ("down", {"down"})):
+        p = oracle.pack_block_gptq(w, dict(diag, **{hk: corr}))
+        differs = {k for k in rtn if not np.array_equal(p[k][0], rtn[k][0])}
+        assert differs == changed, hk
 
 
 # ------------------------------------------------------------ gain folding --
