@@ -119,6 +119,10 @@ class ClockSampler:
 
     def stop(self) -> dict:
         if self.p is None:
+            f = getattr(self, "f", None)
+            if f is not None:
+                f.close()
+                os.unlink(f.name)
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.25)
         self.p.terminate()
@@ -129,6 +133,7 @@ class ClockSampler:
         self.f.flush()
         self.f.seek(0)
         rows = [r.split(", ") for r in self.f.read().strip().splitlines() if r.strip()]
+        self.f.close()
         os.unlink(self.f.name)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]

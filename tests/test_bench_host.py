@@ -91,6 +91,15 @@ def test_clock_sampler_without_nvidia_smi():
     s = object.__new__(bench.ClockSampler)
     s.p = None
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+    s = object.__new__(bench.ClockSampler)
+    s.f, s.p = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False), None
+    assert s.stop()["sm_mhz"] is None and not os.path.exists(s.f.name)  # its sample file is removed
+
+
+def test_clock_sampler_removes_its_sample_file():
+    s = _sampler_with(["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active"])
+    s.stop()
+    assert not os.path.exists(s.f.name)
 
 
 def test_cpu_baseline_names_the_host():
