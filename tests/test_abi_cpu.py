@@ -107,3 +107,15 @@ def test_kv_size_formula(L):
     streams = 2 * 3 * 8 * 1008 * (128 + 4)
     rope = 1008 * 64 * 8
     assert n >= streams + rope and n <= streams + rope + 1024
+
+
+def test_kv_size_beyond_32_bits(L):
+    # a 70B model's whole cache: 80 layers x 32 sequences x 65536 positions,
+    # 8 kv-heads x (128 code bytes + 4 scale bytes) per position -- 177 GB
+    n = futr.futr_kv_size(futr.make_shape(LLAMA70B), 80, 32, 65536)
+    streams = 80 * 32 * 8 * 65536 * (128 + 4)
+    assert streams > 2 ** 32
+    assert streams + 65536 * 64 * 8 <= n <= streams + 65536 * 64 * 8 + 1024
+    # one position more than the supported capacity is refused
+    sz = C.c_size_t(0)
+    assert L.futr_kv_size(C.byref(futr.make_shape(LLAMA70B)), 80, 32, 65537, C.byref(sz)) == futr.FUTR_ERR_UNSUPPORTED
