@@ -113,9 +113,10 @@ int32_t futr_version(void);
 futr_status futr_weights_size(const futr_shape* shape, size_t* bytes);
 
 /*
- * Offline packer (abstract: "folding the fixed RMSNorm gain into weights";
- * "INT4 projection weights", "round-to-nearest weights"; explainer, INT4 Decode
- * section: weights "stored according to the Tensor Core fragment layout").
+ * Offline packer.  The abstract folds the fixed RMSNorm gain into the weights
+ * and quantizes the projection weights to INT4 by rounding to nearest; the
+ * explainer's INT4 Decode section stores them in the tensor cores' fragment
+ * layout.
  *
  * Inputs are fp32 device matrices in nn.Linear layout [out, in], row-major:
  * wq [Hq*d, H], wk/wv [Hkv*d, H], wo [H, Hq*d], wgate/wup [I, H], wdown [H, I],
@@ -155,9 +156,9 @@ futr_status futr_kv_init(const futr_shape* shape, int32_t n_layers, int32_t max_
                          void* stream);
 
 /*
- * INT4 KV-cache copy writer (abstract: "an INT4 KV-cache copy"; "A
- * block-diagonal Hadamard transform reduces cache quantization error from
- * outlier channels").  For sequences seq0 .. seq0+batch-1 of layer `layer`,
+ * INT4 KV-cache copy writer.  The abstract keeps an INT4 copy of the KV cache
+ * and rotates it block-diagonally with a Hadamard matrix, which lowers the
+ * quantization error that outlier channels cause.  For sequences seq0 .. seq0+batch-1 of layer `layer`,
  * append n_tok tokens at positions pos[b] .. pos[b]+n_tok-1 (pos: device int32
  * [batch]).  k, v: bf16 [batch][Hkv][n_tok][d] (already position-encoded).
  * Each (token, kv-head) vector is widened to fp32, rotated by the fp32 fast
@@ -190,8 +191,8 @@ futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int3
                                 void* ws_mem, size_t ws_bytes, futr_ws* ws, void* stream);
 
 /*
- * One decode step of one block for `batch` sequences (abstract: "Decode uses
- * INT4 projection weights and an INT4 KV-cache copy"):
+ * One decode step of one block for `batch` sequences (abstract: decode runs on
+ * INT4 projection weights and the INT4 copy of the KV cache):
  *   r1 = 1/sqrt(mean(x^2)+eps);  [q;k;v] = r1 * (W'qkv x);  RoPE(q, k) at pos[b];
  *   q' = H q / sqrt(n) (fp32); the new k, v are rotated, quantized and stored in
  *   slot pos[b] of the cache (direct KV-cache placement);

@@ -2,9 +2,9 @@
 // read-back.
 //
 // "FuTransformer: FP8 prefill and INT4 decode for Llama-style inference on
-// Hopper", abstract: "Decode uses ... an INT4 KV-cache copy"; "A block-diagonal
-// Hadamard transform reduces cache quantization error from outlier channels";
-// keys follow the Tensor Core fragment layout.  Here keys are stored as the
+// Hopper", abstract: decode reads an INT4 copy of the KV cache, rotated
+// block-diagonally with a Hadamard matrix so that outlier channels cost less
+// quantization error, and keys are stored in the tensor cores' fragment layout.  Here keys are stored as the
 // mma.m16n8k16 B operand of q.k (k = head dims, n = positions) and values as
 // the B operand of p.V (k = positions, n = head dims).
 #include "futr_internal.cuh"

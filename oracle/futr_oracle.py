@@ -39,8 +39,8 @@ Readings of points the pages leave open (the plainest one each time):
     cannot be folded into INT4 codes).  The final gain multiplies the last
     block's output in fp32 and the product is rounded once to bf16, the LM
     head's activation; the RMSNorm factor r (float64 here) scales the logits.
-  * GPTQ "in the same format": the same INT4 codes and one fp16 scale per
-    (output row, 128 inputs), chosen by the published GPTQ column sweep
+  * GPTQ in the same INT4 format ([ABS]): the same INT4 codes and one fp16
+    scale per (output row, 128 inputs), chosen by the published GPTQ column sweep
     (natural column order, 1 % dampening, upper Cholesky factor of the inverse
     Hessian).  Each group's scale follows the rule of the round-to-nearest
     quantizer, applied to the group's error-compensated weights when the sweep
@@ -81,8 +81,8 @@ def bf16_bits_to_float(u) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
-# Hadamard rotation  [EN] Hadamard paragraph; [ABS] "block-diagonal Hadamard
-# transform reduces cache quantization error from outlier channels"
+# Hadamard rotation  [EN] Hadamard paragraph; [ABS] (a block-diagonal Hadamard
+# rotation lowers the cache's quantization error from outlier channels)
 # ----------------------------------------------------------------------------
 
 
@@ -131,8 +131,8 @@ def fwht_f32(v: np.ndarray, n: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
-# INT4 round-to-nearest quantizer  [ABS] "INT4 projection weights", "round-to-
-# nearest weights"; [EN] INT4 Decode section ("INT4 KV-cache copy")
+# INT4 round-to-nearest quantizer  [ABS] (INT4 projection weights rounded to
+# nearest; the INT4 cache copy); [EN] INT4 Decode section
 # ----------------------------------------------------------------------------
 
 FP16_MAX = 65504.0
@@ -177,8 +177,8 @@ def dequant(codes: np.ndarray, scales: np.ndarray, group: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
-# offline weight packing  [ABS] "folding the fixed RMSNorm gain into weights";
-# "INT4 projection weights ... round-to-nearest"
+# offline weight packing  [ABS] (the fixed RMSNorm gain folded into the
+# weights; INT4 projection weights rounded to nearest)
 # ----------------------------------------------------------------------------
 
 
@@ -222,8 +222,9 @@ def dequant_block(packed: Dict[str, tuple], group: int = 128) -> Dict[str, np.nd
 
 
 # ----------------------------------------------------------------------------
-# GPTQ in the same INT4 format  [ABS] "GPTQ in the same format"; the explainer's
-# paragraph on GPTQ (calibration data, approximate second-order information).
+# GPTQ in the same INT4 format  [ABS] (GPTQ codes in the round-to-nearest
+# format); [EN] accuracy section, paragraph on GPTQ (calibration data,
+# approximate second-order information).
 # The pages name the method only; its steps here are those of the published
 # GPTQ algorithm (Frantar et al., "GPTQ: Accurate Post-Training Quantization
 # for Generative Pre-trained Transformers", 2022), without activation reordering.
@@ -300,7 +301,8 @@ def pack_block_gptq(weights: Dict[str, np.ndarray], hessians: Dict[str, np.ndarr
 
 
 # ----------------------------------------------------------------------------
-# KV cache copy  [ABS] "INT4 KV-cache copy"; "block-diagonal Hadamard transform"
+# KV cache copy  [ABS] (the INT4 cache copy and its block-diagonal Hadamard
+# rotation)
 # ----------------------------------------------------------------------------
 
 
@@ -365,9 +367,10 @@ def online_softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale:
 
 
 # ----------------------------------------------------------------------------
-# the decode block, stage by stage  [ABS] "Decode uses INT4 projection weights
-# and an INT4 KV-cache copy"; "The kernels match a quantized reference
-# computation" -- evaluated here on the identical dequantized values.
+# the decode block, stage by stage  [ABS] (decode on INT4 projection weights
+# and the INT4 cache copy; the kernels are checked against a reference that
+# computes on the quantized values) -- evaluated here on the identical
+# dequantized values.
 # ----------------------------------------------------------------------------
 
 
