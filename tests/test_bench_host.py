@@ -30,6 +30,21 @@ def test_block_bytes_8b_batch1_hand_count():
     assert st["attention"] == 8_192 + 1_082_400 + 8_192
 
 
+def test_block_bytes_70b_batch1_hand_count():
+    """70B block, batch 1, 2048 cached positions, counted by hand:
+    weights: QKV 10240x8192: 41,943,040 + 1,310,720;  O 8192x8192: 33,554,432 + 1,048,576;
+      gate/up 57344x8192: 234,881,024 + 7,340,032;  down 8192x28672: 117,440,512 + 3,670,016
+      -> 441,188,352
+    KV: read 2049 positions x 8 kv-heads x 132 = 2,163,744; new token written 8 x 132 = 1,056
+    activations (bf16): x 16,384 x 2 reads, q' 16,384 out + in, o 16,384 out + in, h 16,384 out + 2 in,
+      a 57,344 out + in, y 16,384 out -> 278,528
+    total 443,631,680."""
+    from int4_weight_kv_w4a16_gb300.inputs import LLAMA70B
+    st = bench.stage_bytes(LLAMA70B, [2048])
+    assert sum(st.values()) == 443_631_680
+    assert st["gate_up"] == 234_881_024 + 7_340_032 + 16_384 + 57_344
+
+
 def test_block_bytes_grow_with_context_and_batch():
     one = bench.stage_bytes(TOY, [100])
     # one more cached position of one sequence: Hkv * (d + 4) more KV bytes
