@@ -5,13 +5,21 @@ heads, head_dim 128, SwiGLU 14336), batch 1, 1024 cached positions in the INT4
 rotated KV cache.  A step is one futr_decode_block call (QKV + RoPE + rotation
 + INT4 KV append, attention, O + residual, gate/up + SwiGLU, down + residual).
 
-Timing: the K timed steps are one CUDA-graph replay (5 kernels per step,
-programmatic dependent launch between them), bracketed by CUDA events on the
-capturing stream; steps cycle over distinct copies of the layer (weights and
-cache) totalling more than 4x the L2, so every step streams from HBM.  One
-JSON line on stdout (rank 0).
+Timing: K steps are captured in one CUDA graph (5 kernels per step,
+programmatic dependent launch between them); the graph is replayed R times
+(--reps, default 10), each replay one timed region of exactly K steps between
+CUDA events, bracketed by a barrier and a device synchronize; the value is the
+median (min and max reported).  Steps cycle over distinct copies of the layer
+(weights and cache) totalling more than 4x the L2, so every step streams from
+HBM.  One JSON line on stdout (rank 0).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl futr|reference]
+After the headline workload the same run times the other block and complete
+8B-step workloads (the "sweep" object: 8B batch 8 and 32, 70B batch 1, 8 and
+32, the 32-layer 8B step at batch 1 and 16), each with its roofline fractions,
+clock record and a bounded CPU-oracle sample; --no-sweep skips it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--reps R] [--workload NAME] [--no-sweep]
+                  [--impl futr|reference]
 
 The llama8b_x32_* workloads time the complete model step instead (32 blocks,
 embedding, final norm and bf16 LM head; futr_decode_step, 164 kernels per step).
@@ -203,6 +211,21 @@ def host_info() -> dict:
     return {"cpu_model": model, "blas": blas, "blas_threads": threads}
 
 
+def _cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def _time_oracle_block(x, wdq, cache, pos, shape, budget_s: float, max_steps: int, min_steps: int = 1):
+    import oracle
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_steps and (len(times) < min_steps or time.perf_counter() - t_all < budget_s):
+        t0 = time.perf_counter()
+        oracle.decode_block(x, wdq, cache, pos, shape)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
 def oracle_baseline(wl, budget_s: float = 15.0, max_steps: int = 20, min_steps: int = 1):
     """Time the float64 oracle's decode_block on the host cores, on the same
     workload, for a bounded number of block-steps."""
@@ -216,23 +239,99 @@ def oracle_baseline(wl, budget_s: float = 15.0, max_steps: int = 20, min_steps: 
     hist = inputs.kv_history(shape, lengths, n_outlier=wl.n_outlier, seed=0)
     cache = oracle.build_cache(hist, shape)
     del hist
-    pos = np.asarray(lengths)
-    times = []
-    t_all = time.perf_counter()
-    while len(times) < max_steps and (len(times) < min_steps or time.perf_counter() - t_all < budget_s):
-        t0 = time.perf_counter()
-        oracle.decode_block(x, wdq, cache, pos, shape)
-        times.append(time.perf_counter() - t0)
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": 1e6 * statistics.mean(times), "unit": UNIT, "cores": cores, "kind": "oracle",
+    times = _time_oracle_block(x, wdq, cache, np.asarray(lengths), shape, budget_s, max_steps, min_steps)
+    return {"value": 1e6 * statistics.mean(times), "unit": UNIT, "cores": _cores(), "kind": "oracle",
             "sample": f"{len(times)} full block-steps of {wl.name} (float64 numpy, weights pre-dequantized "
                       f"outside the timed region)", **host_info()}
 
 
+def random_int4_operands(shape, lengths, batch: int, seed: int = 0):
+    """Operands of the oracle's decode_block drawn directly as INT4 codes in
+    [-8, 7] with fp16 scales (weights per 128-input group, cache per token and
+    kv-head): the same shapes as the packed workload without the host-side
+    packing of seeded fp32 weights, which would take minutes at the 70B shape.
+    The oracle's time does not depend on the values."""
+    import oracle
+    r = np.random.default_rng(seed)
+    H, I, d, Hkv = shape.hidden, shape.inter, shape.head_dim, shape.n_kv_heads
+
+    def proj(n, k):
+        c = r.integers(-8, 8, size=(n, k), dtype=np.int8)
+        s = r.uniform(1e-3, 4e-3, size=(n, k // 128)).astype(np.float16)
+        return oracle.dequant(c, s, 128)
+
+    wdq = {"qkv": proj(shape.qkv_rows, H), "o": proj(H, shape.q_rows), "gate": proj(I, H), "up": proj(I, H),
+           "down": proj(H, I)}
+    cache = []
+    for L in lengths:
+        L = int(L)
+        cache.append({"k_codes": r.integers(-8, 8, size=(Hkv, L, d), dtype=np.int8),
+                      "k_scales": r.uniform(0.1, 1.0, size=(Hkv, L)).astype(np.float16),
+                      "v_codes": r.integers(-8, 8, size=(Hkv, L, d), dtype=np.int8),
+                      "v_scales": r.uniform(0.1, 1.0, size=(Hkv, L)).astype(np.float16)})
+    x = inputs.activations(shape, batch, seed)
+    return x, wdq, cache
+
+
+def oracle_sample_baseline(wl, budget_s: float = 4.0, max_steps: int = 5):
+    """The oracle's decode_block on random INT4 operands of this workload's
+    shapes (see random_int4_operands), a bounded number of block-steps."""
+    lengths = inputs.context_lengths(wl)
+    x, wdq, cache = random_int4_operands(wl.shape, lengths, wl.batch)
+    times = _time_oracle_block(x, wdq, cache, np.asarray(lengths), wl.shape, budget_s, max_steps)
+    return {"value": round(1e6 * statistics.mean(times), 1), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"{len(times)} full block-steps of {wl.name} on random INT4 codes and fp16 scales of its "
+                      f"shapes (float64 numpy, weights dequantized outside the timed region)", **host_info()}
+
+
 # ------------------------------------------------------------- GPU bench --
 
+def time_replays(torch, g, reps: int, world: int):
+    """Replay the captured K-step graph `reps` times; each replay is one timed
+    region of exactly K steps between CUDA events on the current stream,
+    bracketed by a barrier and a device synchronize.  ms per replay (max over
+    ranks)."""
+    out = []
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(reps):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        out.append(max_over_ranks(e0.elapsed_time(e1), world))
+    return out
+
+
+def capture(torch, step, steps: int, warmup: int):
+    """W eager warm-up steps, then K steps captured in one CUDA graph, replayed
+    once untimed (uploads the executable graph)."""
+    for k in range(warmup):
+        step(k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            for k in range(steps):
+                step(k)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
+def replay_stats(ms_list, steps: int) -> dict:
+    us = sorted(1000.0 * m / steps for m in ms_list)
+    return {"replays": len(us), "median": round(statistics.median(us), 3), "min": round(us[0], 3),
+            "max": round(us[-1], 3)}
+
+
 class Bench:
-    def __init__(self, wl, device: int):
+    def __init__(self, wl, device: int, device_weights: bool = False):
         import torch
         from int4_weight_kv_w4a16_gb300 import build, futr
         build.build()
@@ -246,24 +345,31 @@ class Bench:
         blob_bytes = futr.futr_weights_size(self.cs)
         l2 = torch.cuda.get_device_properties(device).L2_cache_size
         self.n_copies = max(2, math.ceil(4 * l2 / blob_bytes))
-        w = inputs.block_weights(self.shape, 0)
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
         self.blobs = [futr.alloc_bytes(blob_bytes) for _ in range(self.n_copies)]
-        wd = {k: dev(v) for k, v in w.items()}
+        wd = inputs.block_weights_device(self.shape, 0) if device_weights else \
+            {k: dev(v) for k, v in inputs.block_weights(self.shape, 0).items()}
         futr.futr_pack_weights(self.cs, wd["wq"], wd["wk"], wd["wv"], wd["wo"], wd["wgate"], wd["wup"],
                                wd["wdown"], wd["g_attn"], wd["g_mlp"], self.blobs[0])
-        del wd, w
+        del wd
         for bl in self.blobs[1:]:
             bl.copy_(self.blobs[0])
         self.kv = futr.futr_kv_init(self.cs, self.n_copies, self.b, self.cap,
                                     futr.alloc_bytes(futr.futr_kv_size(self.cs, self.n_copies, self.b, self.cap)))
         self.ws = futr.futr_workspace_init(self.cs, self.b, self.cap,
                                            futr.alloc_bytes(futr.futr_workspace_size(self.cs, self.b, self.cap)))
-        hist = inputs.kv_history(self.shape, self.lengths, n_outlier=wl.n_outlier, seed=0)
-        for layer in range(self.n_copies):
-            for s, (kb, vb) in enumerate(hist):
-                futr.futr_kv_append(self.kv, layer, s, 1, dev(np.array([0], np.int32)), kb.shape[1], dev(kb), dev(vb))
-        del hist
+        zero = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if device_weights:
+            for layer in range(self.n_copies):
+                for s, L in enumerate(self.lengths):
+                    k, v = inputs.kv_history_device(self.shape, int(L), seed=s, n_outlier=wl.n_outlier)
+                    futr.futr_kv_append(self.kv, layer, s, 1, zero, int(L), k, v)
+        else:
+            hist = inputs.kv_history(self.shape, self.lengths, n_outlier=wl.n_outlier, seed=0)
+            for layer in range(self.n_copies):
+                for s, (kb, vb) in enumerate(hist):
+                    futr.futr_kv_append(self.kv, layer, s, 1, zero, kb.shape[1], dev(kb), dev(vb))
+            del hist
         self.x = dev(inputs.activations(self.shape, self.b, 0).view(np.int16))
         self.pos = dev(np.asarray(self.lengths, np.int32))
         self.y = torch.empty_like(self.x)
@@ -279,25 +385,11 @@ class Bench:
         self.futr.futr_decode_block(self.x, self.blobs[layer], self.kv, layer, self.b, self.pos, self.y, self.ws)
 
     def timed(self, steps: int, warmup: int):
-        torch = self.torch
-        for k in range(warmup):
-            self.step(k)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
-                for k in range(steps):
-                    self.step(k)
-        torch.cuda.current_stream().wait_stream(s)
-        g.replay()  # untimed: uploads the executable graph
-        torch.cuda.synchronize()
+        g = capture(self.torch, self.step, steps, warmup)
         st = self.futr.futr_check(self.ws, self.kv)
         if st != 0:
             raise RuntimeError(self.futr.futr_status_string(st))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        return g, e0, e1
+        return g
 
     def stage_times(self, n: int):
         acc = np.zeros(5)
@@ -324,42 +416,46 @@ class Bench:
                 "d2h_bytes_per_step": int(self.b * self.shape.hidden * 2)}
 
 
+def block_point(B, args, world: int, pk: dict) -> dict:
+    """Time one block workload: R replays of the K-step graph, per-kernel event
+    times, and the roofline fractions of the step and of its dominant kernel."""
+    torch = B.torch
+    g = B.timed(args.steps, args.warmup)
+    clocks = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.2)
+    ms = time_replays(torch, g, args.reps, world)
+    clk = clocks.stop()
+    st = B.futr.futr_check(B.ws, B.kv)
+    if st != 0:
+        raise RuntimeError(B.futr.futr_status_string(st))
+    stats = replay_stats(ms, args.steps)
+    us_step = stats["median"]
+    stage_ms = B.stage_times(min(args.steps, 20))
+    total = sum(B.bytes.values())
+    dom = int(np.argmax(stage_ms))
+    dom_name = STAGES[dom]
+    dom_gbs = B.bytes[dom_name] / (stage_ms[dom] * 1e-3) / 1e9
+    return {"ms_list": ms, "stats": stats, "us_step": us_step, "clocks": clk, "stage_ms": stage_ms,
+            "total_bytes": total, "block_gbs": total / (us_step * 1e-6) / 1e9, "dom_name": dom_name,
+            "dom_gbs": dom_gbs, "dom_us": stage_ms[dom] * 1e3, "peak": pk["hbm_gbs"]}
+
+
 def run_futr(args, wl):
     rank, world, local = dist_env()
     import torch
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", init_method="env://")
-    B = Bench(wl, local)
-    g, e0, e1 = B.timed(args.steps, args.warmup)
-    clocks = ClockSampler(local)
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    st = B.futr.futr_check(B.ws, B.kv)
-    if st != 0:
-        raise RuntimeError(B.futr.futr_status_string(st))
-    ms = max_over_ranks(ms, world)
-    us_step = 1000.0 * ms / args.steps
-    value = whole_job_us_per_step(ms, args.steps, world)
-    stage_ms = B.stage_times(min(args.steps, 30))
     pk = peaks()
-    total_bytes = sum(B.bytes.values())
-    dom = int(np.argmax(stage_ms))
-    dom_name = STAGES[dom]
-    dom_gbs = B.bytes[dom_name] / (stage_ms[dom] * 1e-3) / 1e9
+    B = Bench(wl, local)
+    P = block_point(B, args, world, pk)
+    us_step = P["us_step"]
+    value = whole_job_us_per_step(us_step * args.steps / 1000.0, args.steps, world)
     e2e = B.e2e(min(args.steps, 50))
     sh = B.shape
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": False,
+        "warmup": args.warmup, "ms_per_step": round(us_step / 1000.0, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "hidden": sh.hidden, "n_q_heads": sh.n_q_heads, "n_kv_heads": sh.n_kv_heads,
                    "head_dim": sh.head_dim, "inter": sh.inter, "batch": B.b,
@@ -367,21 +463,26 @@ def run_futr(args, wl):
                    if wl.ragged else int(wl.ctx),
                    "weights": "int4 group-128 fp16 scales", "kv_cache": "int4 Hadamard-rotated, fp16 scale per token-head",
                    "l2": f"steps cycle {B.n_copies} distinct layer copies ({B.n_copies * B.blob_bytes / 1e6:.0f} MB of weights) "
-                         f"> 4x L2", "timing": "CUDA graph of K steps, 5 kernels/step, programmatic dependent launch",
+                         f"> 4x L2",
+                   "timing": f"median of {args.reps} timed regions, each exactly K={args.steps} steps of one CUDA "
+                             f"graph (5 kernels/step, programmatic dependent launch)",
                    "parallelism": f"replicas x{world}"},
-        "block_roofline": {"bound": "hbm", "algorithmic_bytes": int(total_bytes),
-                           "achieved": round(total_bytes / (us_step * 1e-6) / 1e9, 1), "peak": pk["hbm_gbs"],
-                           "unit": "GB/s", "frac": round(total_bytes / (us_step * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
-                           "peak_source": pk["source"]},
-        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(dom_gbs / pk["hbm_gbs"], 4),
-                     "traffic": profiled_traffic(dom_name, wl.name),
-                     "algorithmic_bytes": int(B.bytes[dom_name]), "avg_launch_us": round(stage_ms[dom] * 1e3, 3),
+        "replays_us_per_step": P["stats"],
+        "block_roofline": {"bound": "hbm", "algorithmic_bytes": int(P["total_bytes"]),
+                           "achieved": round(P["block_gbs"], 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(P["block_gbs"] / pk["hbm_gbs"], 4), "peak_source": pk["source"]},
+        "roofline": {"kernel": P["dom_name"], "bound": "hbm", "achieved": round(P["dom_gbs"], 1),
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(P["dom_gbs"] / pk["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(P["dom_name"], wl.name),
+                     "algorithmic_bytes": int(B.bytes[P["dom_name"]]), "avg_launch_us": round(P["dom_us"], 3),
                      "peak_source": pk["source"]},
-        "stage_us": {n: round(float(t) * 1e3, 3) for n, t in zip(STAGES, stage_ms)},
+        "stage_us": {n: round(float(t) * 1e3, 3) for n, t in zip(STAGES, P["stage_ms"])},
         "tokens_per_s_blocks_only": round(B.b / (us_step * 1e-6 * N_LAYERS_MODEL.get(sh.hidden, 32)), 1),
-        "e2e": e2e, "clocks": clk, "gpu_launches": 5 * args.steps,
+        "e2e": e2e, "clocks": P["clocks"], "gpu_launches": 5 * args.steps * args.reps,
     }
+    del B
+    if world == 1 and not args.no_sweep:
+        line["sweep"] = run_sweep(args, world, pk)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_baseline(wl)
     if rank == 0:
@@ -393,6 +494,65 @@ def run_futr(args, wl):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+SWEEP = ["llama8b_b8_ctx1024", "llama8b_b32_ragged512-4096", "llama70b_b1_ctx2048", "llama70b_b8_ctx2048",
+         "llama70b_b32_ctx2048", "llama8b_x32_b1_ctx2048", "llama8b_x32_b16_ctx2048"]
+
+
+def run_sweep(args, world: int, pk: dict) -> dict:
+    """The other block and complete-step workloads, each timed like the
+    headline (R regions of exactly K steps) in this run; weights and cache
+    histories drawn on the device.  Each point carries its own clock record
+    and a bounded CPU-oracle sample."""
+    import gc
+    import torch
+    out = {}
+    for name in SWEEP:
+        wl = inputs.WORKLOADS[name]
+        if wl.vocab > 0:
+            B = StepBench(wl, torch.cuda.current_device())
+            g = B.timed(args.steps, args.warmup)
+            clocks = ClockSampler(torch.cuda.current_device())
+            time.sleep(0.2)
+            ms = time_replays(torch, g, args.reps, world)
+            clk = clocks.stop()
+            st = B.futr.futr_check(B.ws, B.kv)
+            if st != 0:
+                raise RuntimeError(B.futr.futr_status_string(st))
+            stats = replay_stats(ms, args.steps)
+            total = sum(B.bytes.values())
+            gbs = total / (stats["median"] * 1e-6) / 1e9
+            rec = {"unit": STEP_UNIT, "us_per_step": stats, "batch": wl.batch, "layers": wl.n_layers,
+                   "tokens_per_s": round(wl.batch / (stats["median"] * 1e-6), 1),
+                   "step_roofline": {"algorithmic_bytes": int(total), "achieved": round(gbs, 1), "unit": "GB/s",
+                                     "frac": round(gbs / pk["hbm_gbs"], 4)},
+                   "clocks": clk}
+            del g, B
+            gc.collect()
+            torch.cuda.empty_cache()
+            if not args.no_cpu_baseline:
+                rec["cpu_baseline"] = step_oracle_sample(wl)
+        else:
+            B = Bench(wl, torch.cuda.current_device(), device_weights=True)
+            P = block_point(B, args, world, pk)
+            rec = {"unit": UNIT, "us_per_step": P["stats"], "batch": wl.batch,
+                   "block_roofline": {"algorithmic_bytes": int(P["total_bytes"]), "achieved": round(P["block_gbs"], 1),
+                                      "unit": "GB/s", "frac": round(P["block_gbs"] / pk["hbm_gbs"], 4)},
+                   "dominant": {"kernel": P["dom_name"], "achieved": round(P["dom_gbs"], 1),
+                                "frac": round(P["dom_gbs"] / pk["hbm_gbs"], 4), "avg_launch_us": round(P["dom_us"], 3)},
+                   "stage_us": {n: round(float(t) * 1e3, 3) for n, t in zip(STAGES, P["stage_ms"])},
+                   "tokens_per_s_blocks_only": round(
+                       wl.batch / (P["us_step"] * 1e-6 * N_LAYERS_MODEL.get(wl.shape.hidden, 32)), 1),
+                   "clocks": P["clocks"]}
+            del B
+            gc.collect()
+            torch.cuda.empty_cache()
+            if not args.no_cpu_baseline:
+                rec["cpu_baseline"] = oracle_sample_baseline(wl)
+        rec["peak_gbs"] = pk["hbm_gbs"]
+        out[name] = rec
+    return out
 
 
 # --------------------------------------------------- complete decode step --
@@ -457,20 +617,7 @@ class StepBench:
                                    self.logits if logits is None else logits, self.ws)
 
     def timed(self, steps: int, warmup: int):
-        torch = self.torch
-        for _ in range(warmup):
-            self.step()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
-                for _ in range(steps):
-                    self.step()
-        torch.cuda.current_stream().wait_stream(s)
-        g.replay()
-        torch.cuda.synchronize()
+        g = capture(self.torch, lambda k: self.step(), steps, warmup)
         st = self.futr.futr_check(self.ws, self.kv)
         if st != 0:
             raise RuntimeError(self.futr.futr_status_string(st))
@@ -529,6 +676,29 @@ def step_oracle_baseline(wl, budget_rows: int = 8192):
             **host_info()}
 
 
+def step_oracle_sample(wl, budget_rows: int = 8192):
+    """As step_oracle_baseline, on random INT4 operands of the block's shapes
+    (random_int4_operands) instead of packed seeded weights."""
+    import oracle
+    sh = wl.shape
+    lengths = inputs.context_lengths(wl)
+    x, wdq, cache = random_int4_operands(sh, lengths, wl.batch)
+    pos = np.asarray(lengths)
+    t_block = min(_time_oracle_block(x, wdq, cache, pos, sh, 0.0, 2, 2))
+    y = oracle.decode_block(x, wdq, cache, pos, sh)["y"]
+    r = np.random.default_rng(0)
+    w_rows = inputs.to_bf16_bits(r.standard_normal((budget_rows, sh.hidden)).astype(np.float32) * 0.02)
+    g = r.uniform(0.5, 1.5, sh.hidden).astype(np.float32)
+    t0 = time.perf_counter()
+    oracle.final_logits(y, g, w_rows, sh.rms_eps)
+    t_head = (time.perf_counter() - t0) * wl.vocab / budget_rows
+    return {"value": round(1e6 * (t_block * wl.n_layers + t_head), 1), "unit": STEP_UNIT, "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"the faster of 2 block-steps of {sh.hidden}-hidden batch {wl.batch} on random INT4 codes and "
+                      f"fp16 scales x {wl.n_layers} layers + final norm and LM head on {budget_rows} of {wl.vocab} "
+                      f"rows scaled to the vocabulary (float64 numpy)", **host_info()}
+
+
 def run_step(args, wl):
     rank, world, local = dist_env()
     import torch
@@ -539,20 +709,14 @@ def run_step(args, wl):
     g = B.timed(args.steps, args.warmup)
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    barrier(world)
+    ms_list = time_replays(torch, g, args.reps, world)
     clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1), world)
     st = B.futr.futr_check(B.ws, B.kv)
     if st != 0:
         raise RuntimeError(B.futr.futr_status_string(st))
-    us_step = 1000.0 * ms / args.steps
+    stats = replay_stats(ms_list, args.steps)
+    us_step = stats["median"]
+    ms = us_step * args.steps / 1000.0
     value = whole_job_us_per_step(ms, args.steps, world)
     pk = peaks()
     total = sum(B.bytes.values())
@@ -565,13 +729,15 @@ def run_step(args, wl):
         "config": {"workload": wl.name, "layers": wl.n_layers, "vocab": wl.vocab, "batch": B.b, "ctx": int(wl.ctx),
                    "weights": "int4 group-128 fp16 scales; bf16 embedding and LM head",
                    "l2": f"{sum(B.bytes.values()) / 1e9:.2f} GB streamed per step > L2",
-                   "timing": "CUDA graph of K steps, 164 kernels/step, programmatic dependent launch",
+                   "timing": f"median of {args.reps} timed regions, each exactly K={args.steps} steps of one CUDA "
+                             f"graph ({2 + 5 * wl.n_layers + 2} kernels/step, programmatic dependent launch)",
                    "parallelism": f"replicas x{world}"},
+        "replays_us_per_step": stats,
         "roofline": {"kernel": "whole step", "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None,
                      "algorithmic_bytes": int(total), "peak_source": pk["source"]},
         "tokens_per_s": round(B.b / (us_step * 1e-6), 1),
-        "e2e": e2e, "clocks": clk, "gpu_launches": (2 + 5 * wl.n_layers + 2) * args.steps,
+        "e2e": e2e, "clocks": clk, "gpu_launches": (2 + 5 * wl.n_layers + 2) * args.steps * args.reps,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = step_oracle_baseline(wl)
@@ -628,6 +794,8 @@ def main():
     ap.add_argument("--impl", default="futr", choices=["futr", "reference"])
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reps", type=int, default=10, help="timed regions of exactly K steps (median reported)")
+    ap.add_argument("--no-sweep", action="store_true", help="time the chosen workload only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -4,6 +4,10 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
 
 #include "futr_internal.cuh"
 #include "proj.cuh"
@@ -53,14 +57,34 @@ struct Plans {
   AttnPlan attn;
 };
 
-Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
+Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int force_attn) {
   const BlobSections sec = blob_sections(s);
-  const int force = env_int("FUTR_SPLITK");
   Plans p;
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
   for (int i = 0; i < 4; ++i) p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
-  p.attn = plan_attention(s, batch, cap, n_sm, env_int("FUTR_ATTN_SPLIT"));
+  p.attn = plan_attention(s, batch, cap, n_sm, force_attn);
   return p;
+}
+
+// Launch plans of one decode call.  FUTR_SPLITK / FUTR_ATTN_SPLIT force the
+// split-K and context-range counts (within the planner's bounds); plans are
+// kept per (shape, batch, capacity, SM count, forced counts), so a repeated
+// call only looks its plan up.
+Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
+  const int force = env_int("FUTR_SPLITK"), force_attn = env_int("FUTR_ATTN_SPLIT");
+  using Key = std::tuple<std::string, int, int, int, int, int>;
+  static std::mutex mu;
+  static std::map<Key, Plans> cache;
+  const Key key(std::string(reinterpret_cast<const char*>(&s), sizeof(s)), batch, cap, n_sm, force, force_attn);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const Plans p = plan_all(s, batch, cap, n_sm, force, force_attn);
+  std::lock_guard<std::mutex> g(mu);
+  if (cache.size() > 4096) cache.clear();
+  return cache.emplace(key, p).first->second;
 }
 
 struct WsLayout {
@@ -80,11 +104,14 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
   L.xin = off; off = align256(off + B * s.hidden * 2);
   L.yout = off; off = align256(off + B * s.hidden * 2);
   L.pos = off; off = align256(off + B * 4);
+  // split records: the largest any plan of a batch up to max_batch can use
+  // (each projection's split cap, independent of occupancy answers and of
+  // forced split counts)
   size_t part = 0, apart = 0;
   for (int b = 1; b <= max_batch; ++b) {
-    const Plans p = make_plans(s, b, cap, n_sm);
+    const Plans p = plan_all(s, b, cap, n_sm, 0, 0);
     for (int i = 0; i < 4; ++i)
-      if (p.proj[i].S > 1 && p.proj[i].part_floats > part) part = p.proj[i].part_floats;
+      if (p.proj[i].s_cap > 1 && p.proj[i].part_cap_floats > part) part = p.proj[i].part_cap_floats;
     if (p.attn.part_floats > apart) apart = p.attn.part_floats;
   }
   L.part = off; L.part_bytes = part * 4; off = align256(off + L.part_bytes);
@@ -168,6 +195,10 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
   base_args.err = err;
   base_args.eps = s.rms_eps;
   unsigned* cnt_next = cnt;
+  // FUTR_TEST_WITHHOLD_COPY=1 (tests of the failure path only): the first CTA
+  // of the QKV projection issues no copy, so its bounded waits run out and the
+  // step reports FUTR_ERR_TIMEOUT
+  const int withhold = env_int("FUTR_TEST_WITHHOLD_COPY") == 1 ? 1 : 0;
 
   cudaError_t e;
   // S2: QKV + RMSNorm factor + RoPE + rotation + INT4 KV placement
@@ -187,6 +218,7 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     A.d = s.head_dim;
     A.nh = s.had_block;
     A.had_c = had_c;
+    A.withhold = withhold;
     if (events) cudaEventRecord(events[0], st);
     e = launch_projection(kEpiQkv, P.proj[0], A, st, pdl);
     if (e != cudaSuccess) return FUTR_ERR_CUDA;
@@ -501,15 +533,22 @@ futr_status futr_check(const futr_ws* ws, const futr_kv* kv, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return FUTR_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return FUTR_ERR_CUDA;
   futr_status result = FUTR_OK;
+  // error regions: word 0 the first error code, word 1 the abort word of the
+  // bounded waits
   int* words[2] = {ws_ok(ws) ? at<int>(ws->base, ws->off_err) : nullptr,
                    kv_ok(kv) ? at<int>(kv->base, kv->err_offset) : nullptr};
   for (int i = 0; i < 2; ++i) {
     if (!words[i]) continue;
-    int v = 0;
-    if (cudaMemcpy(&v, words[i], sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FUTR_ERR_CUDA;
-    if (v != 0) {
-      if (result == FUTR_OK) result = v;
-      if (cudaMemset(words[i], 0, sizeof(int)) != cudaSuccess) return FUTR_ERR_CUDA;
+    int v[2] = {0, 0};
+    if (cudaMemcpy(v, words[i], sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FUTR_ERR_CUDA;
+    if (v[0] != 0 || v[1] != 0) {
+      if (result == FUTR_OK) result = v[0] != 0 ? v[0] : FUTR_ERR_TIMEOUT;
+      if (cudaMemset(words[i], 0, 16) != cudaSuccess) return FUTR_ERR_CUDA;
+      // a launch that gave up on a wait left its split-K arrival counters (and
+      // the persistent kernel's flags) mid-count: start them from zero again
+      if (i == 0 && (v[0] == FUTR_ERR_TIMEOUT || v[1] != 0) && ws->cnt_words > 0 &&
+          cudaMemset(at<uint8_t>(ws->base, ws->off_cnt), 0, ws->cnt_words * 4) != cudaSuccess)
+        return FUTR_ERR_CUDA;
     }
   }
   return result;
@@ -554,6 +593,8 @@ void describe_workspace(const futr_shape& s, int max_batch, int capacity, int n_
 }
 
 int sm_count() { return current_sm_count(); }
+
+bool kv_valid(const futr_kv* kv) { return kv_ok(kv) && shape_ok(&kv->shape) && kv->capacity > 0; }
 
 futr_status check_decode_args(const void* blob, const futr_kv* kv, int layer, int batch, const futr_ws* ws) {
   return check_decode(blob, kv, layer, batch, ws);

@@ -127,12 +127,17 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
   uint64_t* full = reinterpret_cast<uint64_t*>(wl + kMaxCluster * G);
   uint64_t* empty = full + kAttnRing;
 
+  // ring stages the producer issued, and whether some wait of this CTA ran out
+  // (then the CTA lets the issued copies land before it exits)
+  __shared__ int s_issued, s_timeout;
   if (tid == 0) {
     for (int i = 0; i < kAttnRing; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kAttnCW);
     }
     fence_mbar_init();
+    s_issued = 0;
+    s_timeout = 0;
   }
   __syncthreads();
   pdl_trigger();
@@ -178,19 +183,21 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
       };
       const int pre = ntiles < kAttnRing ? ntiles : kAttnRing;
       for (int i = 0; i < pre; ++i) issue(i, i);
-      int slot = 0;
+      int slot = 0, issued = pre;
       uint32_t phase = 0;
       for (int i = kAttnRing; i < ntiles; ++i) {
-        if (!mbar_wait_until(&empty[slot], phase, deadline)) {
-          set_err(a.err, FUTR_ERR_TIMEOUT);
+        if (!mbar_wait_until(&empty[slot], phase, deadline, a.err)) {
+          ok = false;
           break;
         }
         issue(slot, i);
+        issued = i + 1;
         if (++slot == kAttnRing) {
           slot = 0;
           phase ^= 1u;
         }
       }
+      s_issued = issued;
     }
   } else {
     // ----------------------------------------------------------- consumers --
@@ -234,7 +241,7 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
     int slot = 0;
     uint32_t phase = 0;
     for (int i = 0; i < ntiles; ++i) {
-      if (!mbar_wait_until(&full[slot], phase, deadline)) {
+      if (!mbar_wait_until(&full[slot], phase, deadline, a.err)) {
         ok = false;
         break;
       }
@@ -392,7 +399,10 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
       }
     }
   }
-  if (!ok) set_err(a.err, FUTR_ERR_TIMEOUT);
+  if (!ok) {
+    record_timeout(a.err);
+    s_timeout = 1;
+  }
   __syncthreads();
 
   // ---- merge the 4 warps: (mO, mm, ml) of this range
@@ -473,12 +483,13 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
     if (!pos_ok && kvh == 0 && tid == 0) set_err(a.err, FUTR_ERR_OUT_OF_RANGE);
   }
   if (NC > 1) cluster_sync_all();  // the leader is done reading the other CTAs' shared memory
+  if (s_timeout && tid == 0) drain_ring(full, kAttnRing, s_issued);
 }
 
 template <int D, int NTQ>
 cudaError_t configure_attn(int dev) {
-  static unsigned long long configured = 0;  // one bit per device
-  if (configured & (1ull << (dev & 63))) return cudaSuccess;
+  static DeviceOnce configured;
+  if (configured.done(dev)) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, NTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_kernel<D, NTQ>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -486,7 +497,7 @@ cudaError_t configure_attn(int dev) {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_kernel<D, NTQ>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  configured |= 1ull << (dev & 63);
+  configured.mark(dev);
   return cudaSuccess;
 }
 

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -33,6 +34,17 @@ inline int remembered(uint64_t key, Query q) {
   std::lock_guard<std::mutex> g(mu);
   return memo.emplace(key, v).first->second;
 }
+
+// One-time per-device set-up (kernel attributes): one bit per device, set
+// atomically, because host threads may launch on several devices at once.
+// Devices past 63 are set up on every call.
+struct DeviceOnce {
+  std::atomic<uint64_t> bits{0};
+  bool done(int dev) const { return dev >= 0 && dev < 64 && (bits.load(std::memory_order_acquire) >> dev) & 1u; }
+  void mark(int dev) {
+    if (dev >= 0 && dev < 64) bits.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
+};
 
 inline uint64_t occ_key(int dev, int a, int b, size_t smem) {
   return ((uint64_t)(dev & 0xFF) << 56) | ((uint64_t)(a & 0xFF) << 48) | ((uint64_t)(b & 0xFF) << 40) |
@@ -110,7 +122,12 @@ struct BlobHeader {
 };
 
 // ------------------------------------------------------------ PTX helpers --
-constexpr unsigned long long kWaitNs = 1000000000ull;  // bounded waits: 1 s
+// Bounded waits.  Every wait gives up after kWaitNs, or as soon as another CTA
+// of the same launch has recorded a time-out: the error region holds the first
+// error code in word 0 and an abort word in word 1, which record_timeout sets
+// and every waiting loop polls, so one failure ends the whole launch within
+// microseconds instead of each CTA waiting out its own deadline.
+constexpr unsigned long long kWaitNs = 50000000ull;  // 50 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -159,14 +176,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// True once some CTA has recorded a time-out in the error region `err`.
+__device__ __forceinline__ bool aborted(const int* err) {
+  return err && *reinterpret_cast<const volatile int*>(err + 1) != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` until the %globaltimer
-// `deadline` (ns); returns false when it passed (the caller records
-// FUTR_ERR_TIMEOUT and stops waiting).
-__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, unsigned long long deadline) {
+// `deadline` (ns) or until the launch was aborted (see aborted); returns false
+// then (the caller records FUTR_ERR_TIMEOUT and stops waiting).
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, unsigned long long deadline,
+                                                const int* err) {
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 15u && global_ns() > deadline) return false;
+    if ((i & 15u) == 15u && (global_ns() > deadline || aborted(err))) return false;
   }
+}
+
+// After a time-out: wait (bounded, not cut short by the abort word) until the
+// copies of the last `ring` stages issued into a ring of `ring` full barriers
+// have landed, so that no bulk copy still writes into this CTA's shared memory
+// when it exits.  Stage i completes phase i / ring of barrier i % ring; the
+// last `ring` stages are the latest phase of their barriers.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int ring, int issued) {
+  const unsigned long long dl = global_ns() + kWaitNs;
+  for (int i = issued > ring ? issued - ring : 0; i < issued; ++i)
+    mbar_wait_until(&full[i % ring], (uint32_t)(i / ring) & 1u, dl, nullptr);
 }
 
 // Pull [src, src + bytes) into L2 (no completion, no destination).  src
@@ -273,6 +307,14 @@ __device__ __forceinline__ void split_half2(float v0, float v1, uint32_t& hi, ui
 
 __device__ __forceinline__ void set_err(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
+}
+
+// A bounded wait ran out: record the code and raise the abort word that every
+// other wait of the launch polls.
+__device__ __forceinline__ void record_timeout(int* err) {
+  if (!err) return;
+  atomicCAS(err, 0, FUTR_ERR_TIMEOUT);
+  atomicExch(err + 1, 1);
 }
 
 // ------------------------------------------------- rotation + quantizer --

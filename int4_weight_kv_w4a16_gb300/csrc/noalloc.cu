@@ -19,6 +19,7 @@ namespace host {
 uint64_t workspace_bytes(const futr_shape& s, int max_batch, int capacity, int n_sm);
 void describe_workspace(const futr_shape& s, int max_batch, int capacity, int n_sm, void* base, futr_ws* d);
 int sm_count();
+bool kv_valid(const futr_kv* kv);
 futr_status check_decode_args(const void* blob, const futr_kv* kv, int layer, int batch, const futr_ws* ws);
 futr_status launch_block(const uint16_t* x, const void* blob, const futr_kv* kv, int layer, int batch,
                          const int32_t* pos, uint16_t* y, const futr_ws* ws, cudaStream_t st);
@@ -27,9 +28,11 @@ futr_status launch_block(const uint16_t* x, const void* blob, const futr_kv* kv,
 
 namespace {
 
-// 16 MiB: enough for an 8B-shaped block at batch <= 8 with a few thousand
-// cached positions per sequence.  Every device that loads the library keeps
-// this array until the process exits.
+// 16 MiB.  The scratch a call needs depends on the block shape, the batch and
+// the SM count, not on the cache capacity: the 8B-shaped (hidden 4096) and
+// 70B-shaped (hidden 8192) blocks need at most about 10 and 12 MB at batch 32
+// on a 152-SM device.  Every device that loads the library keeps this array
+// until the process exits.
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
@@ -58,7 +61,9 @@ futr_status scratch_address(void** out) {
 extern "C" futr_status futr_decode_block_noalloc(const uint16_t* x, const void* blob, const futr_kv* kv,
                                                  int32_t layer, int32_t batch, const int32_t* pos, uint16_t* y,
                                                  void* stream) {
-  if (!x || !pos || !y || x == y || !kv) return FUTR_ERR_INVALID_ARG;
+  if (!x || !pos || !y || x == y) return FUTR_ERR_INVALID_ARG;
+  // the cache descriptor is checked before its shape sizes anything
+  if (!futr::host::kv_valid(kv)) return FUTR_ERR_INVALID_ARG;
   if (batch < 1 || batch > futr::kMaxBatch) return FUTR_ERR_UNSUPPORTED;
   const int n_sm = futr::host::sm_count();
   if (n_sm <= 0) return FUTR_ERR_CUDA;
@@ -73,8 +78,8 @@ extern "C" futr_status futr_decode_block_noalloc(const uint16_t* x, const void* 
   st = futr::host::check_decode_args(blob, kv, layer, batch, &ws);
   if (st != FUTR_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // the arrival counters and the error word must start at zero; the array
-  // keeps whatever the previous call left
+  // the arrival counters and the error region (error word and abort word)
+  // must start at zero; the array keeps whatever the previous call left
   unsigned char* b = reinterpret_cast<unsigned char*>(base);
   if (cudaMemsetAsync(b + ws.off_cnt, 0, ws.cnt_words * 4, cs) != cudaSuccess) return FUTR_ERR_CUDA;
   if (cudaMemsetAsync(b + ws.off_err, 0, 16, cs) != cudaSuccess) return FUTR_ERR_CUDA;

@@ -37,6 +37,7 @@
 // (tcgen05.mma with A in tensor memory; proj_tc_kernel below).
 #include <cuda.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "futr_internal.cuh"
@@ -144,6 +145,23 @@ __device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, in
     store_v_token<J>(a.kv.stream(n, hg - a.Hq - a.Hkv), a.kv.cap, p, code, s, scratch[warp]);
 }
 
+// The producer lane's count of issued ring stages, for the drain after a
+// time-out: flag[2] = count, flag[3] = 1 once the producer has stopped.
+__device__ __forceinline__ void publish_issued(int* flag, int issued) {
+  reinterpret_cast<volatile int*>(flag)[2] = issued;
+  __threadfence_block();
+  reinterpret_cast<volatile int*>(flag)[3] = 1;
+}
+
+// Wait (bounded) until the producer has stopped; its issued-stage count.
+__device__ __forceinline__ int await_issued(int* flag) {
+  const unsigned long long dl = global_ns() + kWaitNs;
+  while (reinterpret_cast<volatile int*>(flag)[3] == 0 && global_ns() < dl) {
+  }
+  __threadfence_block();
+  return reinterpret_cast<volatile int*>(flag)[2];
+}
+
 __device__ __forceinline__ void tma_2d_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -173,9 +191,9 @@ __device__ __forceinline__ void issue_tile(const ProjArgs& a, const CUtensorMap*
 // Everything after the K-loop: the epilogue tile (filled by write_red from
 // the caller's accumulators), the split record and arrival, the last CTA's
 // reduction and the fused epilogue.  Consumer threads only.
-template <int NT, int EPI, class WriteRed>
+template <int NT, int EPI, class WriteRed, class Drain>
 __device__ __forceinline__ void proj_tail(const ProjArgs& a, uint8_t* smem, int rb, int sk, float* ss, int* flag,
-                                          bool ok, WriteRed&& write_red) {
+                                          bool ok, WriteRed&& write_red, Drain&& drain) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float* red = reinterpret_cast<float*>(smem);  // epilogue [NT*8][kRedLd], aliases the stages
   // the residual rows of this block (RESID): with one batch tile loaded now,
@@ -197,13 +215,19 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, uint8_t* smem, int 
   float2* hcs = reinterpret_cast<float2*>(red + NT * 8 * kRedLd + 4 * kCW * 32);
   int* hpos = reinterpret_cast<int*>(hcs + a.batch * (kRowsPerBlock / a.d) * 64);
   if (!ok) {
-    set_err(a.err, FUTR_ERR_TIMEOUT);
+    record_timeout(a.err);
     flag[1] = 1;
   }
 
   // ------------------------------------------------------------ epilogue --
   consumer_sync();  // every warp is done with the stage ring: reuse it as `red`
-  if (flag[1]) return;  // a wait ran out: the ring may still be in use, write nothing
+  if (flag[1]) {
+    // a wait ran out: write nothing; before leaving, let the producer stop and
+    // the copies it issued land (the arrival counters stay as they are:
+    // futr_check clears them with the time-out it reports)
+    if (tid == 0) drain();
+    return;
+  }
   write_red(red);
   consumer_sync();
 
@@ -381,6 +405,8 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
   if (tid == 0) {
     flag[0] = 0;
     flag[1] = 0;
+    flag[2] = 0;
+    flag[3] = 0;
     for (int i = 0; i < R; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kCW);
@@ -395,7 +421,8 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       const uint32_t tx = kUnitBytes + (kRow1 ? kGroup * 2 : (uint32_t)a.batch * kTileLd * 2);
-      const int pre = ng < R ? ng : R;
+      const bool hold = a.withhold && blockIdx.x == 0;  // test hook: no copy is issued
+      const int pre = hold ? 0 : (ng < R ? ng : R);
       if (!kRow1) prefetch_map(xmap);
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], tx);
@@ -404,22 +431,24 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
       pdl_wait();  // the activations come from the previous kernel
       const unsigned long long deadline = global_ns() + kWaitNs;
       for (int i = 0; i < pre; ++i) issue_tile<kRow1>(a, xmap, stages + (size_t)i * a.stage_bytes, g0 + i, &full[i]);
-      int slot = 0;
+      int slot = 0, issued = pre;
       uint32_t phase = 0;
-      for (int i = R; i < ng; ++i) {
-        if (!mbar_wait_until(&empty[slot], phase, deadline)) {
-          set_err(a.err, FUTR_ERR_TIMEOUT);
+      for (int i = hold ? ng : R; i < ng; ++i) {
+        if (!mbar_wait_until(&empty[slot], phase, deadline, a.err)) {
+          record_timeout(a.err);
           break;
         }
         uint8_t* st = stages + (size_t)slot * a.stage_bytes;
         mbar_arrive_expect_tx(&full[slot], tx);
         bulk_g2s(st, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[slot]);
         issue_tile<kRow1>(a, xmap, st, g0 + i, &full[slot]);
+        issued = i + 1;
         if (++slot == R) {
           slot = 0;
           phase ^= 1u;
         }
       }
+      publish_issued(flag, issued);
     } else {
       pdl_wait();
     }
@@ -459,7 +488,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
   int slot = 0;
   uint32_t phase = 0;
   for (int i = 0; i < ng; ++i) {
-    if (!mbar_wait_until(&full[slot], phase, deadline)) {
+    if (!mbar_wait_until(&full[slot], phase, deadline, a.err)) {
       ok = false;
       break;
     }
@@ -543,21 +572,24 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
     }
   }
   // accumulator fragments -> epilogue tile [batch row][block row]
-  proj_tail<NT, EPI>(a, smem, rb, sk, ss, flag, ok, [&](float* red) {
-    const int t = lane & 3;
+  proj_tail<NT, EPI>(
+      a, smem, rb, sk, ss, flag, ok,
+      [&](float* red) {
+        const int t = lane & 3;
 #pragma unroll
-    for (int m = 0; m < kMT; ++m) {
-      const int r0 = (kMT * warp + m) * 16 + gr;
+        for (int m = 0; m < kMT; ++m) {
+          const int r0 = (kMT * warp + m) * 16 + gr;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int n0 = 8 * nt + 2 * t;
-        red[n0 * kRedLd + r0] = acc[m][nt][0];
-        red[(n0 + 1) * kRedLd + r0] = acc[m][nt][1];
-        red[n0 * kRedLd + r0 + 8] = acc[m][nt][2];
-        red[(n0 + 1) * kRedLd + r0 + 8] = acc[m][nt][3];
-      }
-    }
-  });
+          for (int nt = 0; nt < NT; ++nt) {
+            const int n0 = 8 * nt + 2 * t;
+            red[n0 * kRedLd + r0] = acc[m][nt][0];
+            red[(n0 + 1) * kRedLd + r0] = acc[m][nt][1];
+            red[n0 * kRedLd + r0 + 8] = acc[m][nt][2];
+            red[(n0 + 1) * kRedLd + r0 + 8] = acc[m][nt][3];
+          }
+        }
+      },
+      [&]() { drain_ring(full, R, await_issued(flag)); });
 }
 
 // ------------------------------------------------- tensor-core variant --
@@ -673,6 +705,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   if (tid == 0) {
     flag[0] = 0;
     flag[1] = 0;
+    flag[2] = 0;
+    flag[3] = 0;
     for (int i = 0; i < R; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
@@ -709,22 +743,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       pdl_wait();  // the activations come from the previous kernel
       const unsigned long long deadline = global_ns() + kWaitNs;
       for (int i = 0; i < pre; ++i) tc_issue_tile(stages + (size_t)i * kTcStage, &xmap, g0 + i, &full[i]);
-      int slot = 0;
+      int slot = 0, issued = pre;
       uint32_t phase = 0;
       for (int i = R; i < ng; ++i) {
-        if (!mbar_wait_until(&empty[slot], phase, deadline)) {
-          set_err(a.err, FUTR_ERR_TIMEOUT);
+        if (!mbar_wait_until(&empty[slot], phase, deadline, a.err)) {
+          record_timeout(a.err);
           break;
         }
         uint8_t* st = stages + (size_t)slot * kTcStage;
         mbar_arrive_expect_tx(&full[slot], tx);
         bulk_g2s(st + kTcTile, unit0 + (size_t)i * kUnitBytes, kUnitBytes, &full[slot]);
         tc_issue_tile(st, &xmap, g0 + i, &full[slot]);
+        issued = i + 1;
         if (++slot == R) {
           slot = 0;
           phase ^= 1u;
         }
       }
+      publish_issued(flag, issued);
     } else {
       pdl_wait();
     }
@@ -742,8 +778,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const int slot = i % R, ba = i % 3;
         // the tile has landed; the four consumer warps stored A(i) and read
         // D(i - 2), the previous contents of D[b]
-        if (!mbar_wait_until(&full[slot], (uint32_t)(i / R) & 1u, deadline) ||
-            !mbar_wait_until(&aready[ba], (uint32_t)(i / 3) & 1u, deadline)) {
+        if (!mbar_wait_until(&full[slot], (uint32_t)(i / R) & 1u, deadline, a.err) ||
+            !mbar_wait_until(&aready[ba], (uint32_t)(i / 3) & 1u, deadline, a.err)) {
           ok = false;
           break;
         }
@@ -758,7 +794,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         last_issued[b] = i;
       }
       if (!ok) {
-        set_err(a.err, FUTR_ERR_TIMEOUT);
+        record_timeout(a.err);
         flag[1] = 1;
       }
       __threadfence_block();
@@ -791,7 +827,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (i < ng) {
       const uint8_t* st = stages + (size_t)slot * kTcStage;
       const int ba = i % 3;
-      if (!mbar_wait_until(&full[slot], phase, deadline)) {
+      if (!mbar_wait_until(&full[slot], phase, deadline, a.err)) {
         ok = false;
         break;
       }
@@ -833,7 +869,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       // D of unit i - 2; its buffer is overwritten by the MMAs of unit i,
       // which wait for this warp's arrival below
       const int v = i - 2, bd = v & 1;
-      if (!mbar_wait_until(&mdone[bd], (uint32_t)(v >> 1) & 1u, deadline)) {
+      if (!mbar_wait_until(&mdone[bd], (uint32_t)(v >> 1) & 1u, deadline, a.err)) {
         ok = false;
         break;
       }
@@ -856,7 +892,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     s1 = s0;
   }
   if (!ok) {
-    set_err(a.err, FUTR_ERR_TIMEOUT);
+    record_timeout(a.err);
     flag[1] = 1;
   }
   consumer_sync();
@@ -875,8 +911,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     __syncwarp();
     if (lane < 2 && flag[1]) {
       const int v = *(volatile int*)&last_issued[lane];
-      if (v >= 0 && !mbar_wait_until(&mdone[lane], (uint32_t)(v >> 1) & 1u, global_ns() + kWaitNs))
-        set_err(a.err, FUTR_ERR_TIMEOUT);
+      if (v >= 0 && !mbar_wait_until(&mdone[lane], (uint32_t)(v >> 1) & 1u, global_ns() + kWaitNs, nullptr))
+        record_timeout(a.err);
     }
     __syncwarp();
     tc_fence_after();
@@ -892,10 +928,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
   }
   // thread t holds block row t for batch columns 0..31
-  proj_tail<NT, EPI>(a, smem, rb, sk, ss, flag, ok, [&](float* red) {
+  proj_tail<NT, EPI>(
+      a, smem, rb, sk, ss, flag, ok,
+      [&](float* red) {
 #pragma unroll
-    for (int n = 0; n < 32; ++n) red[n * kRedLd + tid] = acc[n];
-  });
+        for (int n = 0; n < 32; ++n) red[n * kRedLd + tid] = acc[n];
+      },
+      [&]() { drain_ring(full, R, await_issued(flag)); });
 }
 
 template <int NT, int EPI>
@@ -919,8 +958,8 @@ constexpr void (*proj_entry())(ProjArgs, CUtensorMap) {
 
 template <int NT, int EPI>
 cudaError_t configure(int dev) {
-  static unsigned long long configured = 0;  // one bit per device
-  if (configured & (1ull << (dev & 63))) return cudaSuccess;
+  static DeviceOnce configured;
+  if (configured.done(dev)) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(proj_entry<NT, EPI>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kProjMaxSmem);
   if (e != cudaSuccess) return e;
@@ -929,7 +968,7 @@ cudaError_t configure(int dev) {
   e = cudaFuncSetAttribute(proj_entry<NT, EPI>(), cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  configured |= 1ull << (dev & 63);
+  configured.mark(dev);
   return cudaSuccess;
 }
 
@@ -970,14 +1009,14 @@ cudaError_t launch_nt(int nt, const ProjArgs& a, int grid, size_t smem, cudaStre
 
 template <int EPI>
 cudaError_t configure_tc(int dev) {
-  static unsigned long long configured = 0;  // one bit per device
-  if (configured & (1ull << (dev & 63))) return cudaSuccess;
+  static DeviceOnce configured;
+  if (configured.done(dev)) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kProjMaxSmem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(proj_tc_kernel<EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  configured |= 1ull << (dev & 63);
+  configured.mark(dev);
   return cudaSuccess;
 }
 
@@ -1074,12 +1113,18 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   p.off_misc = (ring_bytes + 127) & ~127;
   p.smem = (size_t)p.off_misc + misc + (p.tc ? 1024 : 128);  // the base is rounded up (1024 / 128 bytes)
   // splits: balance waves of resident CTAs; each extra split costs a partial
-  // write and a share of the reduction
+  // write and a share of the reduction.  The search stops at s_cap, which
+  // depends only on the shape, the batch and the SM count (the CTAs that
+  // shared memory admits per SM, not the runtime occupancy answer), so one
+  // workspace size covers every plan: one wave of such CTAs over the row
+  // blocks.
+  const int fit_max = std::max(1, std::min(16, 233472 / (int)(p.smem + 1024)));
+  p.s_cap = std::min(p.n_groups, std::max(1, n_sm * fit_max / p.n_rb));
   const int fit = p.tc ? resident_tc(epi, p.smem) : resident_ctas(batch == 1 ? 0 : p.nt, epi, p.smem);
-  const long long slots = (long long)n_sm * (fit > 0 ? fit : 1);
+  const long long slots = (long long)n_sm * std::min(fit > 0 ? fit : 1, fit_max);
   int best_s = 1;
   double best = 1e30;
-  for (int s = 1; s <= p.n_groups; ++s) {
+  for (int s = 1; s <= p.s_cap; ++s) {
     const long long items = (long long)p.n_rb * s;
     const long long waves = (items + slots - 1) / slots;
     const int per = (p.n_groups + s - 1) / s;
@@ -1089,10 +1134,11 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
       best_s = s;
     }
   }
-  if (force_split > 0) best_s = force_split < p.n_groups ? force_split : p.n_groups;
+  if (force_split > 0) best_s = force_split < p.s_cap ? force_split : p.s_cap;
   p.S = best_s;
   p.rec_floats = batch * kRecLd;
   p.part_floats = (size_t)p.n_rb * p.S * p.rec_floats;
+  p.part_cap_floats = (size_t)p.n_rb * p.s_cap * p.rec_floats;
   return p;
 }
 

@@ -25,6 +25,9 @@ struct ProjArgs {
   unsigned* cnt;                 // arrival counters [n_rb]
   int* err;
   float eps;
+  // failure injection for tests: when 1, CTA 0 issues no copy at all, so its
+  // consumers' bounded waits run out (0 in every normal call)
+  int withhold;
   // RESID / SWIGLU output
   const __nv_bfloat16* resid;    // RESID: [batch][out_ld]
   __nv_bfloat16* out;
@@ -41,10 +44,12 @@ struct ProjArgs {
 
 struct ProjPlan {
   int n_rb, n_groups, nt, S, epi;
+  int s_cap;                     // largest split any plan of this shape and batch can choose
   bool tc;                       // tensor-core kernel (batch 17..32)
   int ring, stage_bytes, off_misc, rec_floats;
   size_t smem;
-  size_t part_floats;
+  size_t part_floats;            // split records of this plan
+  size_t part_cap_floats;        // split records at s_cap (what a workspace reserves)
 };
 
 ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_split, int epi);

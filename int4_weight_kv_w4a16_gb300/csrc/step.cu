@@ -108,12 +108,16 @@ __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const __grid_consta
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * kLmRows, n_st = a.H / kLmK;
 
+  // the producer's issued-stage count and stop flag, for the drain after a time-out
+  __shared__ int s_issued, s_stopped;
   if (tid == 0) {
     for (int i = 0; i < kLmRing; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kLmCW);
     }
     fence_mbar_init();
+    s_issued = 0;
+    s_stopped = 0;
   }
   __syncthreads();
   pdl_trigger();
@@ -129,22 +133,26 @@ __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const __grid_consta
       pdl_wait();  // the activation comes from the previous kernel
       const unsigned long long deadline = global_ns() + kWaitNs;
       for (int i = 0; i < pre; ++i) tma_2d(smem_u32(smem + i * kStage + kLmWBytes), &tx, i * kLmK, 0, &full[i]);
-      int slot = 0;
+      int slot = 0, issued = pre;
       uint32_t phase = 0;
       for (int i = kLmRing; i < n_st; ++i) {
-        if (!mbar_wait_until(&empty[slot], phase, deadline)) {
-          set_err(a.err, FUTR_ERR_TIMEOUT);
+        if (!mbar_wait_until(&empty[slot], phase, deadline, a.err)) {
+          record_timeout(a.err);
           break;
         }
         uint8_t* st = smem + slot * kStage;
         mbar_arrive_expect_tx(&full[slot], kStage);
         tma_2d(smem_u32(st), &tw, i * kLmK, row0, &full[slot]);
         tma_2d(smem_u32(st + kLmWBytes), &tx, i * kLmK, 0, &full[slot]);
+        issued = i + 1;
         if (++slot == kLmRing) {
           slot = 0;
           phase ^= 1u;
         }
       }
+      *reinterpret_cast<volatile int*>(&s_issued) = issued;
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&s_stopped) = 1;
     } else {
       pdl_wait();
     }
@@ -168,7 +176,7 @@ __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const __grid_consta
   uint32_t phase = 0;
   bool ok = true;
   for (int i = 0; i < n_st; ++i) {
-    if (!mbar_wait_until(&full[slot], phase, deadline)) {
+    if (!mbar_wait_until(&full[slot], phase, deadline, a.err)) {
       ok = false;
       break;
     }
@@ -194,7 +202,16 @@ __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const __grid_consta
     }
   }
   if (!ok) {
-    set_err(a.err, FUTR_ERR_TIMEOUT);
+    // let the producer stop and the copies it issued land before leaving
+    record_timeout(a.err);
+    if (lane == 0) {
+      const unsigned long long dl = global_ns() + kWaitNs;
+      while (*reinterpret_cast<volatile int*>(&s_stopped) == 0 && global_ns() < dl) {
+      }
+      __threadfence_block();
+      drain_ring(full, kLmRing, *reinterpret_cast<volatile int*>(&s_issued));
+    }
+    __syncwarp();
     return;
   }
   const int g = lane >> 2, t = lane & 3;
@@ -258,14 +275,14 @@ template <int NT>
 cudaError_t launch_lm_nt(const CUtensorMap& tw, const CUtensorMap& tx, const LmArgs& a, cudaStream_t st, bool pdl) {
   constexpr int kStage = kLmWBytes + 8 * NT * kLmK * 2;
   const size_t smem = (size_t)kLmRing * kStage + 2 * kLmRing * 8 + 1024;  // + alignment slack
-  static unsigned long long configured = 0;  // one bit per device
+  static DeviceOnce configured;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (!(configured & (1ull << (dev & 63)))) {
+  if (!configured.done(dev)) {
     e = cudaFuncSetAttribute(lm_head_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured |= 1ull << (dev & 63);
+    configured.mark(dev);
   }
   return launch_pdl(lm_head_kernel<NT>, dim3((unsigned)(a.vocab / kLmRows)), kLmThreads, smem, st, pdl, tw, tx, a);
 }

@@ -26,11 +26,19 @@ def bits_to_f64(t: torch.Tensor) -> np.ndarray:
     return oracle.bf16_bits_to_float(t.cpu().numpy().view(np.uint16))
 
 
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """The spacing of bf16 values at |v| (8 significant bits): 2^(e - 7) for
+    |v| in [2^e, 2^(e+1)); 0 for v = 0."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 7), 0.0)
+
+
 def assert_close(got: np.ndarray, ref: np.ndarray, name: str, rel=REL_L2, mx=MAX_ABS_RMS, flip=False):
     """rel L2 <= rel and |got - ref| <= mx * rms(ref) elementwise.  flip=True
-    (stage checks of bf16/fp16 outputs) also allows each element one step of
-    the output format (2^-7 of its magnitude): a value that lands within the
-    kernel's fp32 error of a rounding boundary may round the other way."""
+    (stage checks of bf16 outputs) also allows each element one bf16 step at
+    the larger of |got| and |ref|: a value that lands within the kernel's fp32
+    error of a rounding boundary may round the other way."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
@@ -44,10 +52,46 @@ def assert_close(got: np.ndarray, ref: np.ndarray, name: str, rel=REL_L2, mx=MAX
     assert err / nrm <= rel, f"{name}: rel L2 {err / nrm:.3e} > {rel}"
     allowed = mx * rms
     if flip:
-        allowed = np.maximum(allowed, 2.0 ** -7 * np.maximum(np.abs(ref), np.abs(got)))
+        allowed = np.maximum(allowed, bf16_ulp(np.maximum(np.abs(ref), np.abs(got))) * (1 + 1e-12))
     bad = np.abs(got - ref) > allowed
     assert not np.any(bad), f"{name}: max abs {np.abs(got - ref).max():.3e} > allowed ({int(bad.sum())} elements)"
     return {"rel_l2": float(err / nrm), "max_abs_rms": float(np.abs(got - ref).max() / rms)}
+
+
+def _bf16_key(v: np.ndarray) -> np.ndarray:
+    """Order-preserving integer key of bf16 values (adjacent values differ by 1)."""
+    bits = (np.asarray(v, dtype=np.float32).view(np.uint32) >> 16).astype(np.int64)
+    mag = bits & 0x7FFF
+    return np.where(bits & 0x8000, -mag, mag)
+
+
+def assert_rounded(got: np.ndarray, exact: np.ndarray, name: str, tol: float = 2e-5, max_tie_frac: float = 5e-4):
+    """Every bf16 value `got` is the nearest-even rounding of the float64 value
+    `exact`, or -- where `exact` lies within tol * max(|exact|, rms(exact)) of
+    the midpoint between two adjacent bf16 values, i.e. where the kernel's fp32
+    arithmetic decides which way a near-tie rounds -- the other neighbour.  Such
+    ties may make up at most max_tie_frac of the values (at least 4)."""
+    import oracle
+    got = np.asarray(got, dtype=np.float64)
+    exact = np.asarray(exact, dtype=np.float64)
+    assert got.shape == exact.shape, (name, got.shape, exact.shape)
+    assert np.all(np.isfinite(got)), name
+    r = oracle.round_bf16(exact)
+    diff = got != r
+    if not diff.any():
+        return 0
+    scale = np.maximum(np.abs(exact), np.sqrt(np.mean(exact * exact)))
+    near = np.abs(exact - (r + got) / 2) <= tol * scale
+    adjacent = np.abs(_bf16_key(got) - _bf16_key(r)) == 1
+    bad = diff & ~(near & adjacent)
+    if bad.any():
+        i = np.flatnonzero(bad)[0]
+        raise AssertionError(f"{name}: {int(bad.sum())} values are not the rounding of the exact result "
+                             f"(first at flat index {i}: got {got.flat[i]!r}, exact {exact.flat[i]!r}, "
+                             f"nearest {r.flat[i]!r})")
+    ties = int(diff.sum())
+    assert ties <= max(4, int(max_tie_frac * got.size)), f"{name}: {ties} near-tie roundings of {got.size}"
+    return ties
 
 
 def errors(got, ref) -> dict:
@@ -82,7 +126,7 @@ class TieRounding:
             return r
         scale = np.maximum(np.abs(exact), np.sqrt(np.mean(exact * exact)))
         near = np.abs(exact - (r + g) / 2) <= self.tol * scale
-        adjacent = np.abs(g - r) <= 2.0 ** -7 * np.maximum(np.abs(r), np.abs(g)) * (1 + 1e-12)
+        adjacent = np.abs(_bf16_key(g) - _bf16_key(r)) == 1
         take = diff & near & adjacent
         self.ties += int(take.sum())
         return np.where(take, g, r)

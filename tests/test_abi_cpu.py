@@ -119,3 +119,14 @@ def test_kv_size_beyond_32_bits(L):
     # one position more than the supported capacity is refused
     sz = C.c_size_t(0)
     assert L.futr_kv_size(C.byref(futr.make_shape(LLAMA70B)), 80, 32, 65537, C.byref(sz)) == futr.FUTR_ERR_UNSUPPORTED
+
+
+def test_no_alloc_rejects_zeroed_cache_descriptor(L):
+    """A cache descriptor that was never initialised (all zero, so its shape
+    has no kv-heads) is refused before its shape sizes anything."""
+    kv = futr.futr_kv()
+    buf = (C.c_uint16 * 256)()
+    pos = (C.c_int32 * 1)()
+    assert L.futr_decode_block_noalloc(C.addressof(buf), C.addressof(buf), C.byref(kv), 0, 1, C.addressof(pos),
+                                       C.addressof(buf) + 256, None) == futr.FUTR_ERR_INVALID_ARG
+    assert L.futr_decode_block_noalloc(None, None, None, 0, 1, None, None, None) == futr.FUTR_ERR_INVALID_ARG

@@ -124,3 +124,19 @@ def test_cpu_baseline_names_the_host():
     base = bench.oracle_baseline(WORKLOADS["toy_b1_ctx128"], budget_s=0.5, max_steps=3)
     assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] > 0
     assert base["cpu_model"] == info["cpu_model"] and "block-steps of toy_b1_ctx128" in base["sample"]
+
+
+def test_sweep_oracle_sample_on_random_operands():
+    """The sweep's CPU sample times the unmodified oracle on INT4 operands of the
+    workload's shapes drawn directly (codes in [-8, 7], fp16 scales)."""
+    import dataclasses
+    from int4_weight_kv_w4a16_gb300.inputs import WORKLOADS
+    wl = WORKLOADS["toy_b1_ctx128"]
+    x, wdq, cache = bench.random_int4_operands(wl.shape, [128, 5], 2)
+    assert wdq["qkv"].shape == (TOY.qkv_rows, TOY.hidden) and wdq["down"].shape == (TOY.hidden, TOY.inter)
+    assert cache[1]["k_codes"].shape == (TOY.n_kv_heads, 5, TOY.head_dim)
+    assert cache[0]["k_codes"].min() >= -8 and cache[0]["k_codes"].max() <= 7
+    base = bench.oracle_sample_baseline(wl, budget_s=0.2, max_steps=2)
+    assert base["kind"] == "oracle" and base["value"] > 0 and "random INT4 codes" in base["sample"]
+    step = bench.step_oracle_sample(dataclasses.replace(wl, n_layers=2, vocab=256), budget_rows=64)
+    assert step["value"] > 0 and "x 2 layers" in step["sample"]

@@ -223,6 +223,27 @@ def test_decode_8b_b32_ragged():
     run_case(wl.shape, wl.batch, inputs.context_lengths(wl), check_codes=True)
 
 
+def test_decode_8b_b16_ctx1024():
+    """Batch 9-16 on the 8B shape: two batch tiles per mma.sync projection and
+    a 2-D tensor copy of each 16-row activation tile."""
+    run_case(LLAMA8B, 16, [1024 - 37 * i for i in range(16)], seed=16)
+
+
+# hidden 8192 gives gate/up 64 input groups, which sends batch 17-32 to the
+# tensor-core SwiGLU kernel (as at the 70B shape); the other dims are small so
+# the float64 oracle covers every output element of every stage
+WIDE = dataclasses.replace(TOY, hidden=8192, n_q_heads=4, n_kv_heads=2, head_dim=128, inter=1024,
+                           had_block=128)
+
+
+@pytest.mark.parametrize("batch", [17, 24, 32])
+def test_decode_wide_tensor_core_swiglu(batch):
+    r = np.random.default_rng(100 + batch)
+    lengths = list(r.integers(0, 400, size=batch))
+    lengths[0] = 0
+    run_case(WIDE, batch, lengths, seed=batch)
+
+
 def test_decode_deterministic_and_splitk_invariant(monkeypatch):
     shape, batch = TOY, 5
     lengths = [3, 70, 129, 200, 1]
@@ -351,3 +372,44 @@ def test_decode_host_entry_matches_device_entry():
     yh = torch.empty_like(xh).pin_memory()
     futr.futr_decode_block_host(xh, gpu.blob, gpu.kv, 0, batch, ph, yh, gpu.ws)
     np.testing.assert_array_equal(yh.numpy().view(np.uint16), yd)
+
+
+def test_workspace_size_ignores_forced_splits(monkeypatch):
+    """The workspace size is fixed by the shape, the batch and the SM count:
+    forcing split counts changes neither the size nor the ability of a
+    workspace sized without them to run a decode."""
+    cs = futr.make_shape(LLAMA8B)
+    base = {b: futr.futr_workspace_size(cs, b, 4096) for b in (1, 8, 32)}
+    shape, batch = TOY, 4
+    lengths = [3, 70, 129, 0]
+    gpu = GpuBlock(shape, inputs.block_weights(shape, 5), max_batch=batch, capacity=256)
+    gpu.append_history(0, inputs.kv_history(shape, lengths, seed=5))
+    x = inputs.activations(shape, batch, 5)
+    pos = np.array(lengths, np.int32)
+    ref = bits_to_f64(gpu.decode(x, pos))
+    for v in ("1", "7", "300"):
+        monkeypatch.setenv("FUTR_SPLITK", v)
+        monkeypatch.setenv("FUTR_ATTN_SPLIT", v)
+        assert {b: futr.futr_workspace_size(cs, b, 4096) for b in (1, 8, 32)} == base
+        assert_close(bits_to_f64(gpu.decode(x, pos)), ref, f"forced splits {v}", rel=2e-3)
+
+
+def test_wait_timeout_reported_and_recovered(monkeypatch):
+    """A copy that is never issued (test hook) makes the first QKV CTA's bounded
+    waits run out: the step ends, futr_check reports FUTR_ERR_TIMEOUT and resets
+    the workspace's arrival counters, and the next step is exact again."""
+    shape, batch = TOY, 3
+    lengths = [5, 40, 77]
+    gpu = GpuBlock(shape, inputs.block_weights(shape, 6), max_batch=batch, capacity=128)
+    gpu.append_history(0, inputs.kv_history(shape, lengths, seed=6))
+    x = inputs.activations(shape, batch, 6)
+    pos = np.array(lengths, np.int32)
+    ref = gpu.decode(x, pos).cpu().numpy()
+    xd, pd = dev(x.view(np.int16)), dev(pos)
+    for _ in range(2):
+        monkeypatch.setenv("FUTR_TEST_WITHHOLD_COPY", "1")
+        y = torch.empty_like(xd)
+        futr.futr_decode_block(xd, gpu.blob, gpu.kv, 0, batch, pd, y, gpu.ws)
+        assert futr.futr_check(gpu.ws, gpu.kv) == futr.FUTR_ERR_TIMEOUT
+        monkeypatch.delenv("FUTR_TEST_WITHHOLD_COPY")
+        np.testing.assert_array_equal(gpu.decode(x, pos).cpu().numpy(), ref)
