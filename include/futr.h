@@ -89,7 +89,7 @@ typedef struct futr_ws {
   uint64_t off_pos;      /* int32 [b]                                            */
   uint64_t off_part;     /* fp32 split-K partial sums                            */
   uint64_t part_bytes;
-  uint64_t off_apart;    /* reserved: 0 bytes (attention merges on chip)         */
+  uint64_t off_apart;    /* fp32 attention range records (whole-block kernel)    */
   uint64_t apart_bytes;
   uint64_t off_cnt;      /* uint32 arrival counters (self-resetting)             */
   uint64_t cnt_words;
@@ -202,15 +202,19 @@ futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int3
  *   a = bf16(silu(r2 W'gate h) * (r2 W'up h));  y = bf16(h + Wdown a).
  * x, y: bf16 [batch][H] (may not alias).  pos: device int32 [batch], the number
  * of tokens already cached per sequence (sequence b uses cache slot b).
- * blob: packed weights of this layer.  Five kernels, launched back to back with
- * programmatic dependent launch; capturable in a CUDA graph.
+ * blob: packed weights of this layer.  Batch 1..16: one persistent kernel runs
+ * the whole step (all CTAs resident; it assumes no other kernel holds the GPU's
+ * SMs meanwhile, else a bounded wait may report FUTR_ERR_TIMEOUT); batch 17..32,
+ * or with the environment variable FUTR_PERSISTENT=0: five kernels launched
+ * back to back with programmatic dependent launch.  Capturable in a CUDA graph.
  */
 futr_status futr_decode_block(const uint16_t* x, const void* blob, const futr_kv* kv,
                               int32_t layer, int32_t batch, const int32_t* pos, uint16_t* y,
                               const futr_ws* ws, void* stream);
 
-/* As futr_decode_block, with a CUDA event recorded before each of the five
- * kernels and after the last (without programmatic overlap).  Synchronizes
+/* As futr_decode_block run as five kernels at every batch, with a CUDA event
+ * recorded before each kernel and after the last (without programmatic
+ * overlap).  Synchronizes
  * `stream` and writes the five kernel times in milliseconds to
  * stage_ms_host[5] (QKV, attention, O, gate/up, down). */
 futr_status futr_decode_block_timed(const uint16_t* x, const void* blob, const futr_kv* kv,
@@ -235,11 +239,12 @@ futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, con
  * futr_decode_block; x, blob, kv, pos and y are still the caller's.
  *
  * All scratch memory (intermediate activations, partial sums, counters) is a
- * 16 MiB array inside the library that every device loading the library keeps
+ * 48 MiB array inside the library that every device loading the library keeps
  * until exit.  The call allocates nothing and calls no allocating routine.
- * - Returns FUTR_ERR_UNSUPPORTED, launching nothing, when this shape, batch and
- *   the cache's capacity need more than 16 MiB of scratch (the 8B- and
- *   70B-shaped blocks fit at every batch up to 32).
+ * - Returns FUTR_ERR_UNSUPPORTED, launching nothing, when this shape and batch
+ *   need more than 48 MiB of scratch (the size does not depend on the cache's
+ *   capacity; the 8B- and 70B-shaped blocks need about 38 MB at batch 32 on a
+ *   152-SM GPU, less at smaller batches).
  * - The first call on a device resolves the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture.

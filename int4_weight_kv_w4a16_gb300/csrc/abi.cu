@@ -1,6 +1,7 @@
 // C ABI of libfutr.so (declared in include/futr.h): argument checking, memory
 // layouts of the KV cache and the workspace, launch planning, and the five
 // launches of one decode step.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -52,9 +53,15 @@ int env_int(const char* name) {
 
 int round16(int c) { return (c + 15) & ~15; }
 
+int env_int_or(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return v ? std::atoi(v) : dflt;
+}
+
 struct Plans {
   ProjPlan proj[4];  // QKV, O, GU, DOWN
   AttnPlan attn;
+  BlockPlan blk;     // the persistent whole-block kernel (batch <= 16)
 };
 
 Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int force_attn) {
@@ -63,6 +70,7 @@ Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
   for (int i = 0; i < 4; ++i) p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
   p.attn = plan_attention(s, batch, cap, n_sm, force_attn);
+  p.blk = batch <= kBlockMaxBatch ? plan_block(s, batch, cap, n_sm, 0) : BlockPlan{};
   return p;
 }
 
@@ -87,6 +95,17 @@ Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
   return cache.emplace(key, p).first->second;
 }
 
+// Split records per row block that the persistent kernel's projection phase
+// needs when `ne` CTAs share its n_rb x n_groups units in equal contiguous
+// ranges: a row block of n_groups units meets at most n_groups / per + 2 of
+// ranges of at least `per` units.
+int block_stride(int n_rb, int n_groups, int ne) {
+  const long long U = (long long)n_rb * n_groups;
+  const int e = (int)std::min<long long>(ne, U);
+  const int per = (int)(U / e);
+  return std::min(e, n_groups / per + 2);
+}
+
 struct WsLayout {
   uint64_t err, qrot, o, h, a, xin, yout, pos, part, part_bytes, apart, apart_bytes, cnt, cnt_words, total;
 };
@@ -108,17 +127,37 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
   // (each projection's split cap, independent of occupancy answers and of
   // forced split counts)
   size_t part = 0, apart = 0;
+  const BlobSections sec = blob_sections(s);
+  uint64_t n_ctx_max = 0;
   for (int b = 1; b <= max_batch; ++b) {
     const Plans p = plan_all(s, b, cap, n_sm, 0, 0);
     for (int i = 0; i < 4; ++i)
       if (p.proj[i].s_cap > 1 && p.proj[i].part_cap_floats > part) part = p.proj[i].part_cap_floats;
     if (p.attn.part_floats > apart) apart = p.attn.part_floats;
+    if (b <= kBlockMaxBatch) {
+      // the persistent kernel with the most CTAs any plan of this batch uses
+      const BlockPlan bp = plan_block(s, b, cap, n_sm, 0);
+      if (bp.grid_cap > 0) {
+        for (int i = 0; i < 4; ++i) {
+          const int n_rb = sec.rows[i] / kRowsPerBlock, ng = sec.cols[i] / kGroup;
+          const size_t f = (size_t)n_rb * block_stride(n_rb, ng, bp.grid_cap) * b * kRecLd;
+          if (f > part) part = f;
+        }
+        const int tiles = (cap + 63) / 64;
+        const int nc = std::max(1, std::min({(bp.grid_cap + bp.n_ctx - 1) / bp.n_ctx, 32, tiles}));
+        const size_t af = (size_t)bp.n_ctx * nc * bp.arec_floats;
+        if (af > apart) apart = af;
+        if ((uint64_t)bp.n_ctx > n_ctx_max) n_ctx_max = bp.n_ctx;
+      }
+    }
   }
   L.part = off; L.part_bytes = part * 4; off = align256(off + L.part_bytes);
   L.apart = off; L.apart_bytes = apart * 4; off = align256(off + L.apart_bytes);
-  const BlobSections sec = blob_sections(s);
-  uint64_t cnt = 0;  // split-K arrival counters, one per row block of each projection
+  // split-K arrival counters, one per row block of each projection; then the
+  // persistent kernel's context counters and its six phase counters
+  uint64_t cnt = 0;
   for (int i = 0; i < 4; ++i) cnt += sec.rows[i] / kRowsPerBlock;
+  cnt += n_ctx_max + 6;
   L.cnt = off; L.cnt_words = cnt; off = align256(off + cnt * 4);
   L.total = off;
   return L;
@@ -163,16 +202,21 @@ futr_status check_decode(const void* blob, const futr_kv* kv, int layer, int bat
   return FUTR_OK;
 }
 
-// The five kernels of one decode step.  events: NULL, or 6 events recorded
-// around the launches (then launched without programmatic overlap).
+// Use the persistent whole-block kernel for this call?  (FUTR_PERSISTENT=0
+// selects the five kernels.)
+bool use_block_kernel(const Plans& P, int batch) {
+  return batch <= kBlockMaxBatch && P.blk.ok && env_int_or("FUTR_PERSISTENT", 1) != 0;
+}
+
+// One decode step: the persistent whole-block kernel (batch <= 16), or five
+// kernels with programmatic dependent launch.  events: NULL, or 6 events
+// recorded around the five kernels (then launched without programmatic
+// overlap, always as five kernels).
 futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, int layer, int batch,
                       const int32_t* pos, uint16_t* y, const futr_ws* ws, cudaStream_t st,
                       cudaEvent_t* events) {
   const futr_shape& s = ws->shape;
   const Plans P = make_plans(s, batch, kv->capacity, ws->n_sm);
-  for (int i = 0; i < 4; ++i)
-    if (P.proj[i].S > 1 && P.proj[i].part_floats * 4 > ws->part_bytes) return FUTR_ERR_INVALID_ARG;
-  if (P.attn.part_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
   const BlobSections sec = blob_sections(s);
   const uint8_t* wb = reinterpret_cast<const uint8_t*>(blob);
   void* base = ws->base;
@@ -189,104 +233,112 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
   const KvView kvl = kv_layer_view(*kv, layer);
   const float had_c = (float)(1.0 / std::sqrt((double)s.had_block));
 
-  ProjArgs base_args{};
-  base_args.batch = batch;
-  base_args.part = part;
-  base_args.err = err;
-  base_args.eps = s.rms_eps;
+  // the four projections' arguments: QKV (S2), O (S4), gate/up (S5), down (S6)
+  ProjArgs PA[4];
+  const __nv_bfloat16* xin[4] = {xb, o, h, a};
+  const __nv_bfloat16* resid[4] = {nullptr, xb, nullptr, h};
+  __nv_bfloat16* outs[4] = {nullptr, h, a, yb};
+  const int out_ld[4] = {0, s.hidden, s.inter, s.hidden};
   unsigned* cnt_next = cnt;
-  // FUTR_TEST_WITHHOLD_COPY=1 (tests of the failure path only): the first CTA
-  // of the QKV projection issues no copy, so its bounded waits run out and the
-  // step reports FUTR_ERR_TIMEOUT
-  const int withhold = env_int("FUTR_TEST_WITHHOLD_COPY") == 1 ? 1 : 0;
-
-  cudaError_t e;
-  // S2: QKV + RMSNorm factor + RoPE + rotation + INT4 KV placement
-  {
-    ProjArgs A = base_args;
-    A.w = wb + sec.off[0];
-    A.xin = xb;
-    A.K = sec.cols[0];
-    A.cnt = cnt_next;
-    A.blob_magic = reinterpret_cast<const uint64_t*>(blob);
-    A.qrot = qrot;
-    A.kv = kvl;
-    A.pos = pos;
-    A.rope = at<const float2>(kv->base, kv->rope_offset);
-    A.Hq = s.n_q_heads;
-    A.Hkv = s.n_kv_heads;
-    A.d = s.head_dim;
-    A.nh = s.had_block;
-    A.had_c = had_c;
-    A.withhold = withhold;
-    if (events) cudaEventRecord(events[0], st);
-    e = launch_projection(kEpiQkv, P.proj[0], A, st, pdl);
-    if (e != cudaSuccess) return FUTR_ERR_CUDA;
-    cnt_next += P.proj[0].n_rb;
-  }
-  // S3: attention
-  {
-    AttnArgs A{};
-    A.qrot = qrot;
-    A.kv = kvl;
-    A.pos = pos;
+  for (int i = 0; i < 4; ++i) {
+    ProjArgs A{};
+    A.w = wb + sec.off[i];
+    A.xin = xin[i];
+    A.K = sec.cols[i];
     A.batch = batch;
-    A.Hq = s.n_q_heads;
-    A.Hkv = s.n_kv_heads;
-    A.G = s.n_q_heads / s.n_kv_heads;
-    A.nh = s.had_block;
-    A.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
-    A.had_c = had_c;
-    A.out = o;
+    A.part = part;
     A.err = err;
-    if (events) cudaEventRecord(events[1], st);
-    e = launch_attention(P.attn, A, s.head_dim, st, pdl);
-    if (e != cudaSuccess) return FUTR_ERR_CUDA;
-  }
-  // S4: O projection + residual
-  {
-    ProjArgs A = base_args;
-    A.w = wb + sec.off[1];
-    A.xin = o;
-    A.K = sec.cols[1];
+    A.eps = s.rms_eps;
     A.cnt = cnt_next;
-    A.resid = xb;
-    A.out = h;
-    A.out_ld = s.hidden;
-    if (events) cudaEventRecord(events[2], st);
-    e = launch_projection(kEpiResid, P.proj[1], A, st, pdl);
-    if (e != cudaSuccess) return FUTR_ERR_CUDA;
-    cnt_next += P.proj[1].n_rb;
+    cnt_next += sec.rows[i] / kRowsPerBlock;
+    A.resid = resid[i];
+    A.out = outs[i];
+    A.out_ld = out_ld[i];
+    if (i == 0) {
+      A.blob_magic = reinterpret_cast<const uint64_t*>(blob);
+      A.qrot = qrot;
+      A.kv = kvl;
+      A.pos = pos;
+      A.rope = at<const float2>(kv->base, kv->rope_offset);
+      A.Hq = s.n_q_heads;
+      A.Hkv = s.n_kv_heads;
+      A.d = s.head_dim;
+      A.nh = s.had_block;
+      A.had_c = had_c;
+      // FUTR_TEST_WITHHOLD_COPY=1 (tests of the failure path only): the first
+      // CTA of the QKV projection issues no copy, so its bounded waits run
+      // out and the step reports FUTR_ERR_TIMEOUT
+      A.withhold = env_int("FUTR_TEST_WITHHOLD_COPY") == 1 ? 1 : 0;
+    }
+    PA[i] = A;
   }
-  // S5: gate/up + RMSNorm factor + SwiGLU
-  {
-    ProjArgs A = base_args;
-    A.w = wb + sec.off[2];
-    A.xin = h;
-    A.K = sec.cols[2];
-    A.cnt = cnt_next;
-    A.out = a;
-    A.out_ld = s.inter;
-    if (events) cudaEventRecord(events[3], st);
-    e = launch_projection(kEpiSwiglu, P.proj[2], A, st, pdl);
-    if (e != cudaSuccess) return FUTR_ERR_CUDA;
-    cnt_next += P.proj[2].n_rb;
+  AttnArgs AT{};
+  AT.qrot = qrot;
+  AT.kv = kvl;
+  AT.pos = pos;
+  AT.batch = batch;
+  AT.Hq = s.n_q_heads;
+  AT.Hkv = s.n_kv_heads;
+  AT.G = s.n_q_heads / s.n_kv_heads;
+  AT.nh = s.had_block;
+  AT.qk_scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.head_dim));
+  AT.had_c = had_c;
+  AT.out = o;
+  AT.err = err;
+
+  if (!events && use_block_kernel(P, batch)) {
+    const BlockPlan& bp = P.blk;
+    BlockArgs B{};
+    for (int i = 0; i < 4; ++i) {
+      const int n_rb = sec.rows[i] / kRowsPerBlock, ng = sec.cols[i] / kGroup;
+      const long long U = (long long)n_rb * ng;
+      B.pa[i] = PA[i];
+      B.pa[i].rec_floats = batch * kRecLd;
+      B.ph[i].w = PA[i].w;
+      B.ph[i].n_rb = n_rb;
+      B.ph[i].n_groups = ng;
+      B.ph[i].ne = (int)std::min<long long>(bp.grid, U);
+      B.pa[i].part_stride = block_stride(n_rb, ng, B.ph[i].ne);
+      if ((size_t)n_rb * B.pa[i].part_stride * B.pa[i].rec_floats * 4 > ws->part_bytes) return FUTR_ERR_INVALID_ARG;
+    }
+    B.at = AT;
+    B.n_ctx = bp.n_ctx;
+    B.NC = bp.NC;
+    B.nsub = bp.nsub;
+    B.arec_floats = bp.arec_floats;
+    if ((size_t)bp.n_ctx * bp.NC * bp.arec_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
+    B.apart = at<float>(base, ws->off_apart);
+    B.actx = cnt_next;
+    B.done = cnt_next + (size_t)batch * s.n_kv_heads * bp.nsub;
+    if ((uint64_t)(B.done + 6 - cnt) > ws->cnt_words) return FUTR_ERR_INVALID_ARG;
+    B.ring = bp.ring;
+    B.stage_bytes = bp.stage_bytes;
+    B.off_scratch = bp.off_scratch;
+    B.off_misc = bp.off_misc;
+    B.err = err;
+    CUtensorMap maps[4];
+    for (int i = 0; i < 4; ++i)
+      if (!make_proj_tile_map(&maps[i], xin[i], batch, sec.cols[i], batch)) return FUTR_ERR_CUDA;
+    return cuda_status(launch_block(bp, B, maps, st, pdl));
   }
-  // S6: down projection + residual
-  {
-    ProjArgs A = base_args;
-    A.w = wb + sec.off[3];
-    A.xin = a;
-    A.K = sec.cols[3];
-    A.cnt = cnt_next;
-    A.resid = h;
-    A.out = yb;
-    A.out_ld = s.hidden;
-    if (events) cudaEventRecord(events[4], st);
-    e = launch_projection(kEpiResid, P.proj[3], A, st, pdl);
+
+  for (int i = 0; i < 4; ++i)
+    if (P.proj[i].S > 1 && P.proj[i].part_floats * 4 > ws->part_bytes) return FUTR_ERR_INVALID_ARG;
+  if (P.attn.part_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
+  const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
+  cudaError_t e;
+  for (int i = 0; i < 4; ++i) {
+    if (events) cudaEventRecord(events[i == 0 ? 0 : i + 1], st);
+    e = launch_projection(epi[i], P.proj[i], PA[i], st, pdl);
     if (e != cudaSuccess) return FUTR_ERR_CUDA;
-    if (events) cudaEventRecord(events[5], st);
+    if (i == 0) {
+      // S3: attention
+      if (events) cudaEventRecord(events[1], st);
+      e = launch_attention(P.attn, AT, s.head_dim, st, pdl);
+      if (e != cudaSuccess) return FUTR_ERR_CUDA;
+    }
   }
+  if (events) cudaEventRecord(events[5], st);
   return FUTR_OK;
 }
 

@@ -28,12 +28,12 @@ futr_status launch_block(const uint16_t* x, const void* blob, const futr_kv* kv,
 
 namespace {
 
-// 16 MiB.  The scratch a call needs depends on the block shape, the batch and
+// 48 MiB.  The scratch a call needs depends on the block shape, the batch and
 // the SM count, not on the cache capacity: the 8B-shaped (hidden 4096) and
-// 70B-shaped (hidden 8192) blocks need at most about 10 and 12 MB at batch 32
-// on a 152-SM device.  Every device that loads the library keeps this array
-// until the process exits.
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+// 70B-shaped (hidden 8192) blocks need at most about 38 MB at batch 32 on a
+// 152-SM device (mostly split-K partial sums).  Every device that loads the
+// library keeps this array until the process exits.
+constexpr size_t kStaticScratchBytes = size_t(48) << 20;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 

@@ -10,6 +10,8 @@ namespace futr {
 constexpr int kMaxRing = 8;         // bulk-copy ring depth (stages)
 constexpr int kTileLd = 136;        // bf16 row of an activation tile in shared memory (128 + pad)
 constexpr int kRedLd = 132;         // fp32 row of the epilogue tile (bank-conflict padding)
+constexpr int kRecCols = kRowsPerBlock / 4 + 1;  // float4 columns per batch row of a split record
+constexpr int kRecLd = 4 * kRecCols;             // floats per batch row of a split record
 constexpr int kProjMaxSmem = 200 * 1024;
 
 constexpr int kEpiResid = 0;
@@ -20,6 +22,7 @@ struct ProjArgs {
   const uint8_t* w;              // section base of the packed blob
   const __nv_bfloat16* xin;      // activations [batch][K]
   int K, n_groups, S, batch;
+  int part_stride;               // records per row block in `part` (S in the one-projection kernels)
   int ring, stage_bytes, off_misc, rec_floats;
   float* part;                   // split-K partial records [n_rb][S][rec_floats]
   unsigned* cnt;                 // arrival counters [n_rb]
@@ -79,5 +82,42 @@ bool make_proj_tile_map(CUtensorMap* m, const void* x, int rows, int K, int box_
 
 AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int force_split);
 cudaError_t launch_attention(const AttnPlan& p, AttnArgs a, int d, cudaStream_t st, bool pdl);
+
+// ------------------------------------------ persistent whole-block kernel --
+constexpr int kBlockMaxBatch = 16;       // batch tiles 1..2 of mma.sync
+constexpr int kBlockMaxSmem = 227 * 1024;
+
+// One projection phase of the block kernel: its section, row blocks, input
+// groups and the CTAs that take part (each a contiguous range of units).
+struct BlockPhase {
+  const uint8_t* w;
+  int n_rb, n_groups, ne;
+};
+
+struct BlockArgs {
+  ProjArgs pa[4];                // epilogue arguments of QKV, O, gate/up, down
+  BlockPhase ph[4];
+  AttnArgs at;                   // attention (qrot, cache, pos, out = o, ...)
+  int n_ctx, NC, nsub, arec_floats;
+  float* apart;                  // context-range records [n_ctx][NC][arec_floats]
+  unsigned* actx;                // arrival counters [n_ctx] (self-resetting)
+  unsigned* done;                // [6]: completed row blocks / contexts per phase, CTAs that left
+  int ring, stage_bytes, off_scratch, off_misc;
+  int* err;
+};
+
+struct BlockPlan {
+  bool ok;
+  int nt, ntq, nsub, stage_bytes, ring, off_scratch, off_misc;
+  int grid;                      // CTAs of the launch (all resident)
+  int grid_cap;                  // the most any plan of this shape uses (workspace bound)
+  int n_ctx, NC, arec_floats;
+  size_t smem;
+};
+
+// fixed_ctas_per_sm: 0 = the default (two per SM, fewer if the occupancy
+// answer is lower).
+BlockPlan plan_block(const futr_shape& s, int batch, int cap, int n_sm, int fixed_ctas_per_sm);
+cudaError_t launch_block(const BlockPlan& p, const BlockArgs& a, const CUtensorMap* maps, cudaStream_t st, bool pdl);
 
 }  // namespace futr

@@ -65,12 +65,15 @@ def _bf16_key(v: np.ndarray) -> np.ndarray:
     return np.where(bits & 0x8000, -mag, mag)
 
 
-def assert_rounded(got: np.ndarray, exact: np.ndarray, name: str, tol: float = 2e-5, max_tie_frac: float = 5e-4):
-    """Every bf16 value `got` is the nearest-even rounding of the float64 value
-    `exact`, or -- where `exact` lies within tol * max(|exact|, rms(exact)) of
-    the midpoint between two adjacent bf16 values, i.e. where the kernel's fp32
-    arithmetic decides which way a near-tie rounds -- the other neighbour.  Such
-    ties may make up at most max_tie_frac of the values (at least 4)."""
+def assert_rounded(got: np.ndarray, exact: np.ndarray, name: str, tol: float = 2e-5, max_tie_frac: float = 1e-3):
+    """Every bf16 value `got` is a bf16 rounding of a value within
+    tol * max(|exact|, rms(exact)) of the float64 result `exact`: the kernel
+    computes exact with that fp32 error and rounds it to nearest, so
+    |got - exact| <= half a bf16 step + tol * scale.  For values well above
+    tol * rms this admits only the nearest rounding, or its neighbour where
+    exact lies that close to a midpoint; for values near zero it admits the
+    kernel's absolute error.  Values other than the nearest rounding may make
+    up at most max_tie_frac of the values (at least 4)."""
     import oracle
     got = np.asarray(got, dtype=np.float64)
     exact = np.asarray(exact, dtype=np.float64)
@@ -81,9 +84,8 @@ def assert_rounded(got: np.ndarray, exact: np.ndarray, name: str, tol: float = 2
     if not diff.any():
         return 0
     scale = np.maximum(np.abs(exact), np.sqrt(np.mean(exact * exact)))
-    near = np.abs(exact - (r + got) / 2) <= tol * scale
-    adjacent = np.abs(_bf16_key(got) - _bf16_key(r)) == 1
-    bad = diff & ~(near & adjacent)
+    half_step = 0.5 * bf16_ulp(np.maximum(np.abs(got), np.abs(exact)))
+    bad = diff & (np.abs(got - exact) > half_step + tol * scale)
     if bad.any():
         i = np.flatnonzero(bad)[0]
         raise AssertionError(f"{name}: {int(bad.sum())} values are not the rounding of the exact result "

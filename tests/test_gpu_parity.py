@@ -244,7 +244,39 @@ def test_decode_wide_tensor_core_swiglu(batch):
     run_case(WIDE, batch, lengths, seed=batch)
 
 
+@pytest.mark.parametrize("batch", [1, 5, 9, 16])
+def test_decode_toy_five_kernel_path(monkeypatch, batch):
+    """Batch 1..16 runs the persistent whole-block kernel by default; the five
+    one-stage kernels (FUTR_PERSISTENT=0) stay checked at the same batches."""
+    monkeypatch.setenv("FUTR_PERSISTENT", "0")
+    r = np.random.default_rng(500 + batch)
+    lengths = list(r.integers(0, 300, size=batch))
+    run_case(TOY, batch, lengths, seed=batch + 50)
+
+
+def test_decode_8b_b1_five_kernel_path(monkeypatch):
+    monkeypatch.setenv("FUTR_PERSISTENT", "0")
+    run_case(LLAMA8B, 1, [1024], seed=3)
+
+
+def test_decode_persistent_deterministic():
+    """The persistent kernel's split and merge orders are fixed: two runs of
+    the same step are bit-identical (batch 1, 7 and 16)."""
+    for batch in (1, 7, 16):
+        lengths = [(53 * i + 17) % 260 for i in range(batch)]
+        weights = inputs.block_weights(TOY, 21)
+        x = inputs.activations(TOY, batch, 21)
+        hist = inputs.kv_history(TOY, lengths, seed=21)
+        gpu = GpuBlock(TOY, weights, max_batch=batch, capacity=288)
+        gpu.append_history(0, hist)
+        pos = np.array(lengths, np.int32)
+        y0 = gpu.decode(x, pos).cpu().numpy()
+        y1 = gpu.decode(x, pos).cpu().numpy()
+        np.testing.assert_array_equal(y0, y1)
+
+
 def test_decode_deterministic_and_splitk_invariant(monkeypatch):
+    monkeypatch.setenv("FUTR_PERSISTENT", "0")  # forced splits apply to the five-kernel path
     shape, batch = TOY, 5
     lengths = [3, 70, 129, 200, 1]
     weights = inputs.block_weights(shape, 7)
@@ -293,6 +325,7 @@ def test_decode_attention_split_invariant(monkeypatch):
     """The context ranges of a (sequence, kv-head) merge in a thread-block
     cluster: 1, 2, 3 or 4 ranges agree within the block tolerance, and a
     repeated plan is bit-identical."""
+    monkeypatch.setenv("FUTR_PERSISTENT", "0")  # the cluster merge is the five-kernel path's
     shape, batch = TOY, 5
     lengths = [3, 70, 129, 200, 1]
     weights = inputs.block_weights(shape, 11)
@@ -394,10 +427,12 @@ def test_workspace_size_ignores_forced_splits(monkeypatch):
         assert_close(bits_to_f64(gpu.decode(x, pos)), ref, f"forced splits {v}", rel=2e-3)
 
 
-def test_wait_timeout_reported_and_recovered(monkeypatch):
-    """A copy that is never issued (test hook) makes the first QKV CTA's bounded
+@pytest.mark.parametrize("persistent", ["1", "0"], ids=["whole_block", "five_kernels"])
+def test_wait_timeout_reported_and_recovered(monkeypatch, persistent):
+    """A copy that is never issued (test hook) makes the first CTA's bounded
     waits run out: the step ends, futr_check reports FUTR_ERR_TIMEOUT and resets
-    the workspace's arrival counters, and the next step is exact again."""
+    the workspace's counters, and the next step is exact again."""
+    monkeypatch.setenv("FUTR_PERSISTENT", persistent)
     shape, batch = TOY, 3
     lengths = [5, 40, 77]
     gpu = GpuBlock(shape, inputs.block_weights(shape, 6), max_batch=batch, capacity=128)

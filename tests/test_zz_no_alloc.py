@@ -16,7 +16,7 @@ from tests._gpu_helpers import GpuBlock, dev
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_BYTES = 16 * 2**20
+SCRATCH_BYTES = 48 * 2**20
 
 
 def _block(shape, lengths, seed, device_weights=False):
