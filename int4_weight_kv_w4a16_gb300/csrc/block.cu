@@ -487,6 +487,9 @@ __global__ void __launch_bounds__(kBlkThreads, 2)
     fence_mbar_init();
   }
   __syncthreads();
+  // the next launch may place its CTAs as these leave: they stream their
+  // weights at once and wait (griddepcontrol.wait) for this one to finish
+  pdl_trigger();
 
   if (warp == kWarpW) {
     if ((tid & 31) == 0) weight_producer<D>(a, stages, full, empty, pflag);
@@ -555,7 +558,11 @@ cudaError_t launch_t(const BlockPlan& p, const BlockArgs& a, const CUtensorMap* 
 template <int NT, int D, int NTQ>
 int occupancy_t(size_t smem) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || configure_block<NT, D, NTQ>(dev) != cudaSuccess) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (configure_block<NT, D, NTQ>(dev) != cudaSuccess) {
+    cudaGetLastError();  // not left pending for a later call to report
+    return 0;
+  }
   return remembered(occ_key(dev, 16 * NT + NTQ, D, smem), [&]() {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, block_kernel<NT, D, NTQ>, kBlkThreads, smem) !=
@@ -609,7 +616,8 @@ BlockPlan plan_block(const futr_shape& s, int batch, int cap, int n_sm, int fixe
                         127) & ~127;
   // CTAs per SM: two (or as asked), the ring as deep as the shared memory left
   const int per_sm = fixed_ctas_per_sm > 0 ? fixed_ctas_per_sm : 2;
-  const long long budget = 232448 / per_sm - 1024 - 128 - (long long)scratch - kBlkMisc - 256;
+  const long long budget = std::min<long long>(232448 / per_sm - 1024, kBlockMaxSmem - 1024) - 128 -
+                           (long long)scratch - kBlkMisc - 256;
   int ring = (int)(budget / p.stage_bytes);
   ring = std::min(ring, kBlkMaxRing);
   if (ring < 2) return BlockPlan{};

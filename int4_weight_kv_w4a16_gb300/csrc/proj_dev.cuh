@@ -180,7 +180,8 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
     if (EPI == kEpiResid) {
 #pragma unroll
       for (int n = 0; n < NT * 8; ++n)
-        rres[n] = n < a.batch ? a.resid[(size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid]
+        // through L2: in the whole-block kernel another CTA wrote it in this launch
+        rres[n] = n < a.batch ? __ldcg(a.resid + (size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid)
                               : __float2bfloat16_rn(0.f);
     }
   };
