@@ -305,6 +305,7 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     B.n_ctx = bp.n_ctx;
     B.NC = bp.NC;
     B.nsub = bp.nsub;
+    B.gc = bp.gc;
     B.arec_floats = bp.arec_floats;
     if ((size_t)bp.n_ctx * bp.NC * bp.arec_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
     B.apart = at<float>(base, ws->off_apart);

@@ -18,11 +18,15 @@
 //               same code as the one-projection kernels), the attention of
 //               each KV tile (AttnWarp), the split-K / split-context tails and
 //               the fused epilogues;
-//   warp 4      weight producer: one 1-D bulk copy per weight unit; for a KV
-//               tile only an L2 prefetch (the tile may still be written);
-//   warp 5      activation producer: per weight unit its activation tile (2-D
-//               tensor copy), per KV tile its four bulk copies, each phase
-//               only once the previous phase has completed.
+//   warp 4      lane 0, the weight producer: one 1-D bulk copy per weight
+//               unit; for a KV tile only an L2 prefetch (the tile may still be
+//               written); lane 1, the activation producer: per weight unit its
+//               activation tile (2-D tensor copy), per KV tile its four bulk
+//               copies, each phase only once the previous phase has completed
+//               (the two lanes poll their barriers without blocking).
+// Attention works in sub-groups of at most 4 query heads (one n-tile of hi|lo
+// query columns), which keeps the consumers within the register budget of
+// four CTAs per SM.
 // A ring stage holds one weight unit + its activation tile, or one 64-position
 // KV tile; its full barrier expects one arrival from each producer.
 //
@@ -49,8 +53,8 @@ namespace futr {
 namespace {
 
 constexpr int kBlkCW = 4;                        // consumer warps
-constexpr int kWarpW = kBlkCW, kWarpA = kBlkCW + 1;
-constexpr int kBlkThreads = (kBlkCW + 2) * 32;  // + weight producer + activation producer
+constexpr int kWarpP = kBlkCW;                   // the producer warp (lanes 0 and 1)
+constexpr int kBlkThreads = (kBlkCW + 1) * 32;
 constexpr int kBlkMaxRing = 32;
 constexpr int kBlkMaxNC = 32;                   // context ranges per context
 constexpr int kPhQ = 0, kPhA = 1, kPhG = 3;  // phases: QKV, attention, O (2), gate/up, down (4)
@@ -81,6 +85,15 @@ __device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned target,
     if (ld_acquire_gpu(cnt) >= target) return true;
     if ((i & 7u) == 7u && (global_ns() > deadline || aborted(err))) return false;
     __nanosleep(64);
+  }
+}
+
+// As mbar_wait_until with non-blocking tests (the producer lanes share a warp).
+__device__ __forceinline__ bool mbar_poll_until(uint64_t* bar, uint32_t parity, unsigned long long deadline,
+                                                const int* err) {
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 15u) == 15u && (global_ns() > deadline || aborted(err))) return false;
   }
 }
 
@@ -121,148 +134,180 @@ __device__ __forceinline__ AttnItem attn_item(const BlockArgs& a, int j) {
   return it;
 }
 
-// phases Q, O, G, D are projections 0..3
-__device__ __forceinline__ int proj_index(int ph) { return ph == kPhQ ? 0 : ph - 1; }
+// phases Q, O, G, D are projections 0..3; the phase counter a projection's
+// epilogues count, and the one its activation tiles wait for
+constexpr int phase_of(int pi) { return pi == 0 ? kPhQ : pi + 1; }
 
-__device__ __forceinline__ PhaseSplit phase_split(const BlockArgs& a, int ph) {
-  const BlockPhase& P = a.ph[proj_index(ph)];
-  return PhaseSplit{P.n_rb, P.n_groups, P.ne};
+template <int PI>
+__device__ __forceinline__ PhaseSplit phase_split(const BlockArgs& a) {
+  return PhaseSplit{a.ph[PI].n_rb, a.ph[PI].n_groups, a.ph[PI].ne};
 }
 
 // ------------------------------------------------------------ producers --
-// The weight producer: weight units of every projection stage; for a KV tile
-// stage only its arrival (and an L2 prefetch of the tile's history).  Never
-// waits on another CTA.
-template <int D>
-__device__ __noinline__ void weight_producer(const BlockArgs& a, uint8_t* stages, uint64_t* full, uint64_t* empty, int* flag) {
-  const int c = blockIdx.x, R = a.ring;
-  const unsigned long long deadline = global_ns() + kWaitNs;
-  int i = 0;
-  // test hook (failure path): CTA 0 issues nothing, so its consumers' bounded
-  // waits run out
-  bool ok = !(a.pa[0].withhold && c == 0);
-  auto slot_free = [&](int s) {
-    if (s < R) return true;
-    return mbar_wait_until(&empty[s % R], (uint32_t)((s / R) + 1) & 1u, deadline, a.err);
-  };
-  for (int ph = 0; ph < 5 && ok; ++ph) {
-    if (ph == kPhA) {
-      for (int j = c; j < a.n_ctx * a.NC && ok; j += gridDim.x) {
-        const AttnItem it = attn_item(a, j);
-        const uint8_t* strm = a.at.kv.stream(it.b, it.kvh);
-        const int cap = a.at.kv.cap;
-        for (int t = it.t0; t < it.t1; ++t, ++i) {
-          if (!slot_free(i)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive(&full[i % R]);
-          const int c0 = t * kTilePos, n16 = (min(kTilePos, it.L - c0) + 15) & ~15;
-          l2_prefetch(strm + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
-          l2_prefetch(strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
-        }
-      }
-      continue;
+// Both producer lanes walk the same stage sequence as the consumers: the
+// projection phases' units of this CTA, and its attention items' KV tiles.
+struct ProdState {
+  int i;       // ring stage
+  bool ok;
+  unsigned long long deadline;
+};
+
+__device__ __forceinline__ bool slot_free(const BlockArgs& a, uint64_t* empty, ProdState& ps) {
+  if (ps.i < a.ring) return true;
+  return mbar_poll_until(&empty[ps.i % a.ring], (uint32_t)((ps.i / a.ring) + 1) & 1u, ps.deadline, a.err);
+}
+
+// The weight producer's part of projection phase PI: one bulk copy per unit.
+template <int PI>
+__device__ __forceinline__ void w_proj(const BlockArgs& a, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                       ProdState& ps) {
+  const PhaseSplit sp = phase_split<PI>(a);
+  const int c = blockIdx.x;
+  if (!ps.ok || c >= sp.ne) return;
+  const uint8_t* w = a.ph[PI].w;
+  for (int u = sp.lo(c), u1 = sp.lo(c + 1); u < u1; ++u, ++ps.i) {
+    if (!slot_free(a, empty, ps)) {
+      ps.ok = false;
+      return;
     }
-    const PhaseSplit sp = phase_split(a, ph);
-    if (c >= sp.ne) continue;
-    const int u0 = sp.lo(c), u1 = sp.lo(c + 1);
-    const uint8_t* w = a.ph[proj_index(ph)].w;
-    for (int u = u0; u < u1; ++u, ++i) {
-      if (!slot_free(i)) {
-        ok = false;
-        break;
+    const int slot = ps.i % a.ring;
+    mbar_arrive_expect_tx(&full[slot], kUnitBytes);
+    bulk_g2s(stages + (size_t)slot * a.stage_bytes, w + (size_t)u * kUnitBytes, kUnitBytes, &full[slot]);
+  }
+}
+
+// The weight producer's part of the attention phase: its arrival on each KV
+// tile stage, and an L2 prefetch of the tile (the new token may still be
+// written: the copy into the stage comes from the activation producer).
+template <int D>
+__device__ __forceinline__ void w_attn(const BlockArgs& a, uint64_t* full, uint64_t* empty, ProdState& ps) {
+  for (int j = blockIdx.x; j < a.n_ctx * a.NC && ps.ok; j += gridDim.x) {
+    const AttnItem it = attn_item(a, j);
+    const uint8_t* strm = a.at.kv.stream(it.b, it.kvh);
+    for (int t = it.t0; t < it.t1; ++t, ++ps.i) {
+      if (!slot_free(a, empty, ps)) {
+        ps.ok = false;
+        return;
       }
-      mbar_arrive_expect_tx(&full[i % R], kUnitBytes);
-      bulk_g2s(stages + (size_t)(i % R) * a.stage_bytes, w + (size_t)u * kUnitBytes, kUnitBytes, &full[i % R]);
+      mbar_arrive(&full[ps.i % a.ring]);
+      const int c0 = t * kTilePos, n16 = (min(kTilePos, it.L - c0) + 15) & ~15;
+      l2_prefetch(strm + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
+      l2_prefetch(strm + (size_t)a.at.kv.cap * (D / 2) + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
     }
   }
-  if (!ok && !(a.pa[0].withhold && c == 0)) record_timeout(a.err);
-  reinterpret_cast<volatile int*>(flag)[2] = i;  // stages this producer arrived on
+}
+
+// The weight producer: never waits on another CTA.
+template <int D>
+__device__ __forceinline__ void weight_producer(const BlockArgs& a, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                                int* flag) {
+  // test hook (failure path): CTA 0 issues nothing, so its consumers' bounded
+  // waits run out
+  const bool hold = a.pa[0].withhold && blockIdx.x == 0;
+  ProdState ps{0, !hold, global_ns() + kWaitNs};
+  w_proj<0>(a, stages, full, empty, ps);
+  w_attn<D>(a, full, empty, ps);
+  w_proj<1>(a, stages, full, empty, ps);
+  w_proj<2>(a, stages, full, empty, ps);
+  w_proj<3>(a, stages, full, empty, ps);
+  if (!ps.ok && !hold) record_timeout(a.err);
+  reinterpret_cast<volatile int*>(flag)[2] = ps.i;  // stages this producer arrived on
   __threadfence_block();
   reinterpret_cast<volatile int*>(flag)[3] = 1;
 }
 
-// The activation producer: per projection stage its activation tile, per KV
-// tile stage its four bulk copies; a phase's first copy waits until the
-// previous phase has completed.
-template <int D>
-__device__ __noinline__ void act_producer(const BlockArgs& a, const CUtensorMap* const* maps, uint8_t* stages, uint64_t* full,
-                             uint64_t* empty, int* flag) {
-  using Lay = AttnLayout<D>;
-  const int c = blockIdx.x, R = a.ring;
-  for (int m = 0; m < 4; ++m) prefetch_map(maps[m]);
-  pdl_wait();  // x comes from the previous kernel
-  const unsigned long long deadline = global_ns() + kWaitNs;
-  int i = 0;
-  bool ok = true;
-  auto slot_free = [&](int s) {
-    if (s < R) return true;
-    return mbar_wait_until(&empty[s % R], (uint32_t)((s / R) + 1) & 1u, deadline, a.err);
-  };
-  // the count that completes the phase before `ph`
-  auto ready = [&](int ph) {
-    if (ph == kPhQ) return true;
-    const int prev = ph - 1;
-    const unsigned target = prev == kPhA ? (unsigned)a.n_ctx : (unsigned)a.ph[proj_index(prev)].n_rb;
-    if (!wait_count(&a.done[prev], target, deadline, a.err)) return false;
-    fence_proxy_async_global();  // the copies below read what other CTAs wrote
-    return true;
-  };
-  for (int ph = 0; ph < 5 && ok; ++ph) {
-    if (ph == kPhA) {
-      bool waited = false;
-      for (int j = c; j < a.n_ctx * a.NC && ok; j += gridDim.x) {
-        const AttnItem it = attn_item(a, j);
-        if (it.t1 > it.t0 && !waited) {
-          if (!ready(ph)) {
-            ok = false;
-            break;
-          }
-          waited = true;
-        }
-        const uint8_t* strm = a.at.kv.stream(it.b, it.kvh);
-        const int cap = a.at.kv.cap;
-        for (int t = it.t0; t < it.t1; ++t, ++i) {
-          if (!slot_free(i)) {
-            ok = false;
-            break;
-          }
-          const int c0 = t * kTilePos, n16 = (min(kTilePos, it.L - c0) + 15) & ~15;  // c0 + n16 <= cap
-          const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
-          uint8_t* st = stages + (size_t)(i % R) * a.stage_bytes;
-          uint64_t* bar = &full[i % R];
-          mbar_arrive_expect_tx(bar, 2 * cb + 2 * sb);
-          bulk_g2s(st, strm + (size_t)c0 * (D / 2), cb, bar);
-          bulk_g2s(st + Lay::kCodes, strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), cb, bar);
-          bulk_g2s(st + 2 * Lay::kCodes, strm + (size_t)cap * D + 2 * (size_t)c0, sb, bar);
-          bulk_g2s(st + 2 * Lay::kCodes + 2 * kTilePos, strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0,
-                   sb, bar);
-        }
-      }
-      continue;
-    }
-    const PhaseSplit sp = phase_split(a, ph);
-    if (c >= sp.ne) continue;
-    const int u0 = sp.lo(c), u1 = sp.lo(c + 1);
-    if (u1 > u0 && !ready(ph)) {
-      ok = false;
-      break;
-    }
-    const CUtensorMap* map = maps[proj_index(ph)];
-    const uint32_t tx = (uint32_t)a.at.batch * kTileLd * 2;
-    for (int u = u0; u < u1; ++u, ++i) {
-      if (!slot_free(i)) {
-        ok = false;
-        break;
-      }
-      const int g = u % sp.n_groups;
-      mbar_arrive_expect_tx(&full[i % R], tx);
-      tma_2d_box(stages + (size_t)(i % R) * a.stage_bytes + kUnitBytes, map, kGroup * g, 0, &full[i % R]);
+// Wait until the phase before one (counter `cnt` of phase `prev` reached
+// `target`), then order the tensor copies after what other CTAs wrote.
+__device__ __forceinline__ bool phase_ready(const BlockArgs& a, int prev, unsigned target, ProdState& ps) {
+  if (!wait_count(&a.done[prev], target, ps.deadline, a.err)) return false;
+  fence_proxy_async_global();
+  return true;
+}
+
+// The activation producer's part of projection phase PI: one tensor copy of
+// the activation tile per unit, once the previous phase has completed.
+template <int PI>
+__device__ __forceinline__ void a_proj(const BlockArgs& a, const CUtensorMap* map, uint8_t* stages, uint64_t* full,
+                                       uint64_t* empty, ProdState& ps) {
+  const PhaseSplit sp = phase_split<PI>(a);
+  const int c = blockIdx.x;
+  if (!ps.ok || c >= sp.ne) return;
+  const int u0 = sp.lo(c), u1 = sp.lo(c + 1);
+  if (u1 <= u0) return;
+  if (PI > 0) {
+    // O waits for every context of attention, gate/up for O, down for gate/up
+    const unsigned target = PI == 1 ? (unsigned)a.n_ctx : (unsigned)a.ph[PI - 1].n_rb;
+    if (!phase_ready(a, phase_of(PI) - 1, target, ps)) {
+      ps.ok = false;
+      return;
     }
   }
-  if (!ok) record_timeout(a.err);
-  reinterpret_cast<volatile int*>(flag + 4)[0] = i;
+  const uint32_t tx = (uint32_t)a.at.batch * kTileLd * 2;
+  for (int u = u0; u < u1; ++u, ++ps.i) {
+    if (!slot_free(a, empty, ps)) {
+      ps.ok = false;
+      return;
+    }
+    const int slot = ps.i % a.ring;
+    mbar_arrive_expect_tx(&full[slot], tx);
+    tma_2d_box(stages + (size_t)slot * a.stage_bytes + kUnitBytes, map, kGroup * (u % sp.n_groups), 0, &full[slot]);
+  }
+}
+
+// The activation producer's part of the attention phase: the four bulk copies
+// of each KV tile, once every QKV row block (queries and new tokens) is done.
+template <int D>
+__device__ __forceinline__ void a_attn(const BlockArgs& a, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                                       ProdState& ps) {
+  using Lay = AttnLayout<D>;
+  bool waited = false;
+  for (int j = blockIdx.x; j < a.n_ctx * a.NC && ps.ok; j += gridDim.x) {
+    const AttnItem it = attn_item(a, j);
+    if (it.t1 > it.t0 && !waited) {
+      if (!phase_ready(a, kPhQ, (unsigned)a.ph[0].n_rb, ps)) {
+        ps.ok = false;
+        return;
+      }
+      waited = true;
+    }
+    const uint8_t* strm = a.at.kv.stream(it.b, it.kvh);
+    const int cap = a.at.kv.cap;
+    for (int t = it.t0; t < it.t1; ++t, ++ps.i) {
+      if (!slot_free(a, empty, ps)) {
+        ps.ok = false;
+        return;
+      }
+      const int c0 = t * kTilePos, n16 = (min(kTilePos, it.L - c0) + 15) & ~15;  // c0 + n16 <= cap
+      const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
+      uint8_t* st = stages + (size_t)(ps.i % a.ring) * a.stage_bytes;
+      uint64_t* bar = &full[ps.i % a.ring];
+      mbar_arrive_expect_tx(bar, 2 * cb + 2 * sb);
+      bulk_g2s(st, strm + (size_t)c0 * (D / 2), cb, bar);
+      bulk_g2s(st + Lay::kCodes, strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), cb, bar);
+      bulk_g2s(st + 2 * Lay::kCodes, strm + (size_t)cap * D + 2 * (size_t)c0, sb, bar);
+      bulk_g2s(st + 2 * Lay::kCodes + 2 * kTilePos, strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb,
+               bar);
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void act_producer(const BlockArgs& a, const CUtensorMap* mx, const CUtensorMap* mo,
+                                             const CUtensorMap* mh, const CUtensorMap* ma, uint8_t* stages,
+                                             uint64_t* full, uint64_t* empty, int* flag) {
+  prefetch_map(mx);
+  prefetch_map(mo);
+  prefetch_map(mh);
+  prefetch_map(ma);
+  pdl_wait();  // x comes from the previous kernel
+  ProdState ps{0, true, global_ns() + kWaitNs};
+  a_proj<0>(a, mx, stages, full, empty, ps);
+  a_attn<D>(a, stages, full, empty, ps);
+  a_proj<1>(a, mo, stages, full, empty, ps);
+  a_proj<2>(a, mh, stages, full, empty, ps);
+  a_proj<3>(a, ma, stages, full, empty, ps);
+  if (!ps.ok) record_timeout(a.err);
+  reinterpret_cast<volatile int*>(flag + 4)[0] = ps.i;
   __threadfence_block();
   reinterpret_cast<volatile int*>(flag + 4)[1] = 1;
 }
@@ -286,11 +331,11 @@ __device__ __forceinline__ void give_stage(const BlockArgs& a, uint64_t* empty, 
 // One attention item: context range it of context ctx; leaves its (m, l, O)
 // record and, as the context's last range, merges the context.
 template <int D, int NTQ>
-__device__ __noinline__ void attn_work(const BlockArgs& a, const AttnItem& it, int ctx, uint8_t* stages,
+__device__ __forceinline__ void attn_work(const BlockArgs& a, const AttnItem& it, int ctx, uint8_t* stages,
                                        float* scratch, int* flag, uint64_t* full, uint64_t* empty,
                                        unsigned long long deadline, ConsumerState& cs) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = attn_gc(a.at.G);
+  const int G = a.gc;  // heads per sub-group (at most 4)
   uint2* qf = reinterpret_cast<uint2*>(scratch);                       // [D/16][NTQ][32]
   float* cm = reinterpret_cast<float*>(qf + (D / 16) * NTQ * 32);      // [warps][G]
   float* cl = cm + kBlkCW * G;                                         // [warps][G]
@@ -369,13 +414,13 @@ __device__ __noinline__ void attn_work(const BlockArgs& a, const AttnItem& it, i
   if (tid == 0) red_release_add(&a.done[kPhA], 1u);
 }
 
-// One projection item: this CTA's units [ua, ub) of row block rb of phase ph
-// (contributor `slot` of S), then the split-K tail and, as the last
-// contributor, the epilogue.
-template <int NT, int EPI>
-__device__ __noinline__ void proj_work(const BlockArgs& a, int ph, int rb, int ua, int ub, int S, int slot,
-                                       uint8_t* stages, float* scratch, float* ss, int* flag, uint64_t* full,
-                                       uint64_t* empty, unsigned long long deadline, ConsumerState& cs) {
+// One projection item: this CTA's units [ua, ub) of row block rb of
+// projection PI (contributor `slot` of S), then the split-K tail and, as the
+// last contributor, the epilogue.
+template <int NT, int EPI, int PI>
+__device__ __forceinline__ void proj_work(const BlockArgs& a, int rb, int ua, int ub, int S, int slot,
+                                          uint8_t* stages, float* scratch, float* ss, int* flag, uint64_t* full,
+                                          uint64_t* empty, unsigned long long deadline, ConsumerState& cs) {
   const int tid = threadIdx.x, lane = tid & 31;
   int xrow[NT];
 #pragma unroll
@@ -406,64 +451,68 @@ __device__ __noinline__ void proj_work(const BlockArgs& a, int ph, int rb, int u
   }
   if (EPI != kEpiResid) ssq_to_smem<NT>(ssq, ss, a.at.batch);
   proj_tail<NT, EPI>(
-      a.pa[proj_index(ph)], scratch, rb, S, slot, ss, flag, ok, [&](float* red) { acc_to_red<NT>(acc, red); },
+      a.pa[PI], scratch, rb, S, slot, ss, flag, ok, [&](float* red) { acc_to_red<NT>(acc, red); },
       [&]() {
         fence_proxy_async_global();  // the outputs are read by other CTAs' tensor copies
         consumer_sync();
-        if (tid == 0) red_release_add(&a.done[ph], 1u);
+        if (tid == 0) red_release_add(&a.done[phase_of(PI)], 1u);
       });
   consumer_sync();  // the scratch is free again
   if (flag[1]) cs.ok = false;
 }
 
-template <int NT, int D, int NTQ>
-__device__ void consumers(const BlockArgs& a, uint8_t* stages, float* scratch, float* ss, int* flag, uint64_t* full,
-                          uint64_t* empty) {
+// The consumers' part of projection phase PI: this CTA's part of each row
+// block its unit range touches.
+template <int NT, int EPI, int PI>
+__device__ __forceinline__ void c_proj(const BlockArgs& a, uint8_t* stages, float* scratch, float* ss, int* flag,
+                                       uint64_t* full, uint64_t* empty, unsigned long long deadline,
+                                       ConsumerState& cs) {
+  const PhaseSplit sp = phase_split<PI>(a);
   const int c = blockIdx.x;
+  if (!cs.ok || c >= sp.ne) return;
+  const int u0 = sp.lo(c), u1 = sp.lo(c + 1), ng = sp.n_groups;
+  for (int rb = u0 / ng; rb * ng < u1 && cs.ok; ++rb) {
+    const int first = sp.owner(rb * ng), last = sp.owner((rb + 1) * ng - 1);
+    proj_work<NT, EPI, PI>(a, rb, max(u0, rb * ng), min(u1, (rb + 1) * ng), last - first + 1, c - first, stages,
+                           scratch, ss, flag, full, empty, deadline, cs);
+  }
+}
+
+template <int NT, int D>
+__device__ __forceinline__ void consumers(const BlockArgs& a, uint8_t* stages, float* scratch, float* ss, int* flag,
+                                          uint64_t* full, uint64_t* empty) {
   pdl_wait();
   const unsigned long long deadline = global_ns() + kWaitNs;
   ConsumerState cs{0, true};
-  for (int ph = 0; ph < 5 && cs.ok; ++ph) {
-    if (ph == kPhA) {
-      bool qready = false;
-      for (int j = c; j < a.n_ctx * a.NC && cs.ok; j += gridDim.x) {
-        if (!qready) {  // the rotated queries and the new tokens' cache entries
-          if (!wait_count(&a.done[kPhQ], (unsigned)a.ph[0].n_rb, deadline, a.err)) {
-            cs.ok = false;
-            break;
-          }
-          qready = true;
-        }
-        attn_work<D, NTQ>(a, attn_item(a, j), j / a.NC, stages, scratch, flag, full, empty, deadline, cs);
+  c_proj<NT, kEpiQkv, 0>(a, stages, scratch, ss, flag, full, empty, deadline, cs);
+  // attention: after every QKV row block (rotated queries, new cache entries)
+  bool qready = false;
+  for (int j = blockIdx.x; j < a.n_ctx * a.NC && cs.ok; j += gridDim.x) {
+    if (!qready) {
+      if (!wait_count(&a.done[kPhQ], (unsigned)a.ph[0].n_rb, deadline, a.err)) {
+        cs.ok = false;
+        break;
       }
-      continue;
+      qready = true;
     }
-    // projection items: this CTA's part of each row block it touches
-    const PhaseSplit sp = phase_split(a, ph);
-    if (c >= sp.ne) continue;
-    const int u0 = sp.lo(c), u1 = sp.lo(c + 1);
-    for (int rb = u0 / sp.n_groups; rb * sp.n_groups < u1 && cs.ok; ++rb) {
-      const int ua = max(u0, rb * sp.n_groups), ub = min(u1, (rb + 1) * sp.n_groups);
-      const int first = sp.owner(rb * sp.n_groups), last = sp.owner((rb + 1) * sp.n_groups - 1);
-      if (ph == kPhQ)
-        proj_work<NT, kEpiQkv>(a, ph, rb, ua, ub, last - first + 1, c - first, stages, scratch, ss, flag, full, empty,
-                               deadline, cs);
-      else if (ph == kPhG)
-        proj_work<NT, kEpiSwiglu>(a, ph, rb, ua, ub, last - first + 1, c - first, stages, scratch, ss, flag, full,
-                                  empty, deadline, cs);
-      else
-        proj_work<NT, kEpiResid>(a, ph, rb, ua, ub, last - first + 1, c - first, stages, scratch, ss, flag, full,
-                                 empty, deadline, cs);
-    }
+    attn_work<D, 1>(a, attn_item(a, j), j / a.NC, stages, scratch, flag, full, empty, deadline, cs);
   }
+  c_proj<NT, kEpiResid, 1>(a, stages, scratch, ss, flag, full, empty, deadline, cs);
+  c_proj<NT, kEpiSwiglu, 2>(a, stages, scratch, ss, flag, full, empty, deadline, cs);
+  c_proj<NT, kEpiResid, 3>(a, stages, scratch, ss, flag, full, empty, deadline, cs);
   if (!cs.ok) {
     record_timeout(a.err);
     flag[1] = 1;
   }
 }
 
-template <int NT, int D, int NTQ>
-__global__ void __launch_bounds__(kBlkThreads, 2)
+// Resident CTAs per SM the register budget is set for: three with one batch
+// tile (at most 136 registers a thread), two with two.
+template <int NT>
+constexpr int kBlkPerSm = NT == 1 ? 3 : 2;
+
+template <int NT, int D>
+__global__ void __launch_bounds__(kBlkThreads, kBlkPerSm<NT>)
     block_kernel(const __grid_constant__ BlockArgs a, const __grid_constant__ CUtensorMap map_x,
                  const __grid_constant__ CUtensorMap map_o, const __grid_constant__ CUtensorMap map_h,
                  const __grid_constant__ CUtensorMap map_a) {
@@ -491,15 +540,13 @@ __global__ void __launch_bounds__(kBlkThreads, 2)
   // weights at once and wait (griddepcontrol.wait) for this one to finish
   pdl_trigger();
 
-  if (warp == kWarpW) {
-    if ((tid & 31) == 0) weight_producer<D>(a, stages, full, empty, pflag);
-  } else if (warp == kWarpA) {
-    if ((tid & 31) == 0) {
-      const CUtensorMap* maps[4] = {&map_x, &map_o, &map_h, &map_a};
-      act_producer<D>(a, maps, stages, full, empty, pflag);
-    }
+  if (warp == kWarpP) {
+    if ((tid & 31) == 0)
+      weight_producer<D>(a, stages, full, empty, pflag);
+    else if ((tid & 31) == 1)
+      act_producer<D>(a, &map_x, &map_o, &map_h, &map_a, stages, full, empty, pflag);
   } else {
-    consumers<NT, D, NTQ>(a, stages, scratch, ss, pflag, full, empty);
+    consumers<NT, D>(a, stages, scratch, ss, pflag, full, empty);
   }
   __syncthreads();
   if (tid == 0) {
@@ -521,26 +568,26 @@ __global__ void __launch_bounds__(kBlkThreads, 2)
   }
 }
 
-template <int NT, int D, int NTQ>
+template <int NT, int D>
 cudaError_t configure_block(int dev) {
   static DeviceOnce configured;
   if (configured.done(dev)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(block_kernel<NT, D, NTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(block_kernel<NT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kBlockMaxSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(block_kernel<NT, D, NTQ>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(block_kernel<NT, D>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   configured.mark(dev);
   return cudaSuccess;
 }
 
-template <int NT, int D, int NTQ>
+template <int NT, int D>
 cudaError_t launch_t(const BlockPlan& p, const BlockArgs& a, const CUtensorMap* maps, cudaStream_t st, bool pdl) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = configure_block<NT, D, NTQ>(dev);
+  e = configure_block<NT, D>(dev);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
@@ -552,20 +599,20 @@ cudaError_t launch_t(const BlockPlan& p, const BlockArgs& a, const CUtensorMap* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, block_kernel<NT, D, NTQ>, a, maps[0], maps[1], maps[2], maps[3]);
+  return cudaLaunchKernelEx(&cfg, block_kernel<NT, D>, a, maps[0], maps[1], maps[2], maps[3]);
 }
 
-template <int NT, int D, int NTQ>
+template <int NT, int D>
 int occupancy_t(size_t smem) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (configure_block<NT, D, NTQ>(dev) != cudaSuccess) {
+  if (configure_block<NT, D>(dev) != cudaSuccess) {
     cudaGetLastError();  // not left pending for a later call to report
     return 0;
   }
-  return remembered(occ_key(dev, 16 * NT + NTQ, D, smem), [&]() {
+  return remembered(occ_key(dev, 16 * NT + 1, D, smem), [&]() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, block_kernel<NT, D, NTQ>, kBlkThreads, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, block_kernel<NT, D>, kBlkThreads, smem) !=
         cudaSuccess) {
       cudaGetLastError();
       return 0;
@@ -574,23 +621,20 @@ int occupancy_t(size_t smem) {
   });
 }
 
-// The instantiations: batch tiles 1..2 (batch <= 16), head dim 64 or 128,
-// 1 or 2 query n-tiles.
-#define FUTR_BLOCK_DISPATCH(NT_, D_, NTQ_, CALL)                                                      \
-  do {                                                                                            \
-    if (D_ == 128) {                                                                              \
-      if (NT_ == 1) { if (NTQ_ == 1) return CALL(1, 128, 1); return CALL(1, 128, 2); }            \
-      if (NTQ_ == 1) return CALL(2, 128, 1);                                                      \
-      return CALL(2, 128, 2);                                                                     \
-    }                                                                                             \
-    if (NT_ == 1) { if (NTQ_ == 1) return CALL(1, 64, 1); return CALL(1, 64, 2); }                \
-    if (NTQ_ == 1) return CALL(2, 64, 1);                                                         \
-    return CALL(2, 64, 2);                                                                        \
+// The instantiations: batch tiles 1..2 (batch <= 16), head dim 64 or 128.
+#define FUTR_BLOCK_DISPATCH(NT_, D_, CALL)                   \
+  do {                                                     \
+    if (D_ == 128) {                                       \
+      if (NT_ == 1) return CALL(1, 128);                   \
+      return CALL(2, 128);                                 \
+    }                                                      \
+    if (NT_ == 1) return CALL(1, 64);                      \
+    return CALL(2, 64);                                    \
   } while (0)
 
-int occupancy_any(int nt, int D, int ntq, size_t smem) {
-#define FUTR_OCC_CALL(A, B, C) occupancy_t<A, B, C>(smem)
-  FUTR_BLOCK_DISPATCH(nt, D, ntq, FUTR_OCC_CALL);
+int occupancy_any(int nt, int D, size_t smem) {
+#define FUTR_OCC_CALL(A, B) occupancy_t<A, B>(smem)
+  FUTR_BLOCK_DISPATCH(nt, D, FUTR_OCC_CALL);
 #undef FUTR_OCC_CALL
 }
 
@@ -599,10 +643,13 @@ int occupancy_any(int nt, int D, int ntq, size_t smem) {
 BlockPlan plan_block(const futr_shape& s, int batch, int cap, int n_sm, int fixed_ctas_per_sm) {
   BlockPlan p{};
   if (batch < 1 || batch > kBlockMaxBatch) return p;
-  const int D = s.head_dim, G = s.n_q_heads / s.n_kv_heads, gc = attn_gc(G), ntq = gc <= 4 ? 1 : 2;
+  // attention sub-groups of at most 4 query heads (one query n-tile)
+  const int D = s.head_dim, G = s.n_q_heads / s.n_kv_heads, nsub = (G + 3) / 4, gc = (G + nsub - 1) / nsub,
+            ntq = 1;
   p.nt = (batch + 7) / 8;
   p.ntq = ntq;
-  p.nsub = attn_nsub(G);
+  p.nsub = nsub;
+  p.gc = gc;
   // scratch: the projection epilogue (tile, split-sum groups, QKV RoPE factors)
   // or the attention work (query fragments, warp partials, merge), whichever
   // is larger
@@ -614,8 +661,9 @@ BlockPlan plan_block(const futr_shape& s, int batch, int cap, int n_sm, int fixe
   p.stage_bytes = (int)(std::max<size_t>(kUnitBytes + (size_t)batch * kTileLd * 2,
                                          D == 128 ? AttnLayout<128>::kStage : AttnLayout<64>::kStage) +
                         127) & ~127;
-  // CTAs per SM: two (or as asked), the ring as deep as the shared memory left
-  const int per_sm = fixed_ctas_per_sm > 0 ? fixed_ctas_per_sm : 2;
+  // CTAs per SM: three up to batch 8, two beyond (or as asked); the ring as
+  // deep as the shared memory left
+  const int per_sm = fixed_ctas_per_sm > 0 ? fixed_ctas_per_sm : (batch <= 8 ? 3 : 2);
   const long long budget = std::min<long long>(232448 / per_sm - 1024, kBlockMaxSmem - 1024) - 128 -
                            (long long)scratch - kBlkMisc - 256;
   int ring = (int)(budget / p.stage_bytes);
@@ -625,7 +673,7 @@ BlockPlan plan_block(const futr_shape& s, int batch, int cap, int n_sm, int fixe
   p.off_scratch = ring * p.stage_bytes;
   p.off_misc = p.off_scratch + (int)scratch;
   p.smem = (size_t)p.off_misc + kBlkMisc + 128;  // the base is rounded up to 128 bytes
-  const int fit = occupancy_any(p.nt, D, ntq, p.smem);
+  const int fit = occupancy_any(p.nt, D, p.smem);
   const int ctas = std::min(per_sm, fit);
   p.grid = n_sm * std::max(ctas, 0);
   p.grid_cap = n_sm * per_sm;
@@ -639,8 +687,8 @@ BlockPlan plan_block(const futr_shape& s, int batch, int cap, int n_sm, int fixe
 }
 
 cudaError_t launch_block(const BlockPlan& p, const BlockArgs& a, const CUtensorMap* maps, cudaStream_t st, bool pdl) {
-#define FUTR_LAUNCH_CALL(A, B, C) launch_t<A, B, C>(p, a, maps, st, pdl)
-  FUTR_BLOCK_DISPATCH(p.nt, a.at.kv.d, p.ntq, FUTR_LAUNCH_CALL);
+#define FUTR_LAUNCH_CALL(A, B) launch_t<A, B>(p, a, maps, st, pdl)
+  FUTR_BLOCK_DISPATCH(p.nt, a.at.kv.d, FUTR_LAUNCH_CALL);
 #undef FUTR_LAUNCH_CALL
 }
 

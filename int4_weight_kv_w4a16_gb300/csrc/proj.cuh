@@ -98,7 +98,7 @@ struct BlockArgs {
   ProjArgs pa[4];                // epilogue arguments of QKV, O, gate/up, down
   BlockPhase ph[4];
   AttnArgs at;                   // attention (qrot, cache, pos, out = o, ...)
-  int n_ctx, NC, nsub, arec_floats;
+  int n_ctx, NC, nsub, gc, arec_floats;  // contexts = sequence x kv-head x sub-group of gc query heads
   float* apart;                  // context-range records [n_ctx][NC][arec_floats]
   unsigned* actx;                // arrival counters [n_ctx] (self-resetting)
   unsigned* done;                // [6]: completed row blocks / contexts per phase, CTAs that left
@@ -108,7 +108,7 @@ struct BlockArgs {
 
 struct BlockPlan {
   bool ok;
-  int nt, ntq, nsub, stage_bytes, ring, off_scratch, off_misc;
+  int nt, ntq, nsub, gc, stage_bytes, ring, off_scratch, off_misc;
   int grid;                      // CTAs of the launch (all resident)
   int grid_cap;                  // the most any plan of this shape uses (workspace bound)
   int n_ctx, NC, arec_floats;
