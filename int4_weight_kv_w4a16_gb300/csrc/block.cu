@@ -57,7 +57,7 @@ constexpr int kWarpP = kBlkCW;                   // the producer warp (lanes 0 a
 constexpr int kBlkThreads = (kBlkCW + 1) * 32;
 constexpr int kBlkMaxRing = 32;
 constexpr int kBlkMaxNC = 32;                   // context ranges per context
-constexpr int kPhQ = 0, kPhA = 1, kPhG = 3;  // phases: QKV, attention, O (2), gate/up, down (4)
+constexpr int kPhQ = 0, kPhA = 1;  // phases: QKV, attention, O (2), gate/up (3), down (4)
 static_assert(kBlkCW == kCW && kBlkCW == kAttnCW, "one consumer thread per output row / four 16-position sub-tiles");
 
 // misc area (after the scratch): ss [32] floats, flag [4] ints, full and
@@ -85,15 +85,6 @@ __device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned target,
     if (ld_acquire_gpu(cnt) >= target) return true;
     if ((i & 7u) == 7u && (global_ns() > deadline || aborted(err))) return false;
     __nanosleep(64);
-  }
-}
-
-// As mbar_wait_until with non-blocking tests (the producer lanes share a warp).
-__device__ __forceinline__ bool mbar_poll_until(uint64_t* bar, uint32_t parity, unsigned long long deadline,
-                                                const int* err) {
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((i & 15u) == 15u && (global_ns() > deadline || aborted(err))) return false;
   }
 }
 
@@ -143,173 +134,169 @@ __device__ __forceinline__ PhaseSplit phase_split(const BlockArgs& a) {
   return PhaseSplit{a.ph[PI].n_rb, a.ph[PI].n_groups, a.ph[PI].ne};
 }
 
-// ------------------------------------------------------------ producers --
-// Both producer lanes walk the same stage sequence as the consumers: the
-// projection phases' units of this CTA, and its attention items' KV tiles.
-struct ProdState {
-  int i;       // ring stage
-  bool ok;
-  unsigned long long deadline;
+// ------------------------------------------------------------- producer --
+// One thread feeds the ring.  It walks this CTA's stage sequence (the units of
+// its range in each projection phase, the KV tiles of its attention items)
+// with two cursors: the weight cursor issues each weight unit's bulk copy (for
+// a KV tile stage only its arrival and an L2 prefetch: the new token may not
+// be written yet) and never waits on another CTA; the activation cursor issues
+// each stage's activation tile or KV-tile copies once the phase before has
+// completed.  Both advance in one loop of non-blocking tests, so neither can
+// hold the other up.
+struct Cursor {
+  int seg;                  // 0 QKV, 1 attention, 2 O, 3 gate/up, 4 down, 5 past the end
+  int u, u1;                // projection: the units [u, u1) still to go
+  int j, t, t1, L, b, kvh;  // attention: item j, its tiles [t, t1)
 };
 
-__device__ __forceinline__ bool slot_free(const BlockArgs& a, uint64_t* empty, ProdState& ps) {
-  if (ps.i < a.ring) return true;
-  return mbar_poll_until(&empty[ps.i % a.ring], (uint32_t)((ps.i / a.ring) + 1) & 1u, ps.deadline, a.err);
-}
+__device__ __forceinline__ int seg_proj(int seg) { return seg == 0 ? 0 : seg - 1; }
 
-// The weight producer's part of projection phase PI: one bulk copy per unit.
-template <int PI>
-__device__ __forceinline__ void w_proj(const BlockArgs& a, uint8_t* stages, uint64_t* full, uint64_t* empty,
-                                       ProdState& ps) {
-  const PhaseSplit sp = phase_split<PI>(a);
+// Move to the first stage at or after segment k.seg (attention: from item k.j).
+__device__ __forceinline__ void cursor_settle(const BlockArgs& a, Cursor& k) {
   const int c = blockIdx.x;
-  if (!ps.ok || c >= sp.ne) return;
-  const uint8_t* w = a.ph[PI].w;
-  for (int u = sp.lo(c), u1 = sp.lo(c + 1); u < u1; ++u, ++ps.i) {
-    if (!slot_free(a, empty, ps)) {
-      ps.ok = false;
-      return;
-    }
-    const int slot = ps.i % a.ring;
-    mbar_arrive_expect_tx(&full[slot], kUnitBytes);
-    bulk_g2s(stages + (size_t)slot * a.stage_bytes, w + (size_t)u * kUnitBytes, kUnitBytes, &full[slot]);
-  }
-}
-
-// The weight producer's part of the attention phase: its arrival on each KV
-// tile stage, and an L2 prefetch of the tile (the new token may still be
-// written: the copy into the stage comes from the activation producer).
-template <int D>
-__device__ __forceinline__ void w_attn(const BlockArgs& a, uint64_t* full, uint64_t* empty, ProdState& ps) {
-  for (int j = blockIdx.x; j < a.n_ctx * a.NC && ps.ok; j += gridDim.x) {
-    const AttnItem it = attn_item(a, j);
-    const uint8_t* strm = a.at.kv.stream(it.b, it.kvh);
-    for (int t = it.t0; t < it.t1; ++t, ++ps.i) {
-      if (!slot_free(a, empty, ps)) {
-        ps.ok = false;
+  while (k.seg < 5) {
+    if (k.seg == 1) {
+      for (; k.j < a.n_ctx * a.NC; k.j += gridDim.x) {
+        const AttnItem it = attn_item(a, k.j);
+        if (it.t1 > it.t0) {
+          k.t = it.t0;
+          k.t1 = it.t1;
+          k.L = it.L;
+          k.b = it.b;
+          k.kvh = it.kvh;
+          return;
+        }
+      }
+    } else {
+      const BlockPhase& P = a.ph[seg_proj(k.seg)];
+      const PhaseSplit sp{P.n_rb, P.n_groups, P.ne};
+      if (c < sp.ne && sp.lo(c) < sp.lo(c + 1)) {
+        k.u = sp.lo(c);
+        k.u1 = sp.lo(c + 1);
         return;
       }
-      mbar_arrive(&full[ps.i % a.ring]);
-      const int c0 = t * kTilePos, n16 = (min(kTilePos, it.L - c0) + 15) & ~15;
-      l2_prefetch(strm + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
-      l2_prefetch(strm + (size_t)a.at.kv.cap * (D / 2) + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
     }
+    ++k.seg;
+    k.j = c;
   }
 }
 
-// The weight producer: never waits on another CTA.
+__device__ __forceinline__ void cursor_next(const BlockArgs& a, Cursor& k) {
+  if (k.seg == 1) {
+    if (++k.t < k.t1) return;
+    k.j += gridDim.x;
+  } else {
+    if (++k.u < k.u1) return;
+    ++k.seg;
+    k.j = blockIdx.x;
+  }
+  cursor_settle(a, k);
+}
+
+// Stage `s` of the ring is free again (its previous use was released).
+__device__ __forceinline__ bool stage_free(const BlockArgs& a, uint64_t* empty, int s) {
+  return s < a.ring || mbar_test_wait(&empty[s % a.ring], (uint32_t)((s / a.ring) + 1) & 1u);
+}
+
 template <int D>
-__device__ __forceinline__ void weight_producer(const BlockArgs& a, uint8_t* stages, uint64_t* full, uint64_t* empty,
-                                                int* flag) {
+__device__ __forceinline__ void issue_weight(const BlockArgs& a, const Cursor& k, int s, uint8_t* stages,
+                                             uint64_t* full) {
+  const int slot = s % a.ring;
+  if (k.seg == 1) {
+    mbar_arrive(&full[slot]);
+    const uint8_t* strm = a.at.kv.stream(k.b, k.kvh);
+    const int c0 = k.t * kTilePos, n16 = (min(kTilePos, k.L - c0) + 15) & ~15;
+    l2_prefetch(strm + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
+    l2_prefetch(strm + (size_t)a.at.kv.cap * (D / 2) + (size_t)c0 * (D / 2), (uint32_t)n16 * (D / 2));
+    return;
+  }
+  mbar_arrive_expect_tx(&full[slot], kUnitBytes);
+  bulk_g2s(stages + (size_t)slot * a.stage_bytes, a.ph[seg_proj(k.seg)].w + (size_t)k.u * kUnitBytes, kUnitBytes,
+           &full[slot]);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_act(const BlockArgs& a, const Cursor& k, int s, uint8_t* stages,
+                                          uint64_t* full, const CUtensorMap* const* maps) {
+  using Lay = AttnLayout<D>;
+  const int slot = s % a.ring;
+  uint8_t* st = stages + (size_t)slot * a.stage_bytes;
+  if (k.seg == 1) {
+    const uint8_t* strm = a.at.kv.stream(k.b, k.kvh);
+    const int cap = a.at.kv.cap;
+    const int c0 = k.t * kTilePos, n16 = (min(kTilePos, k.L - c0) + 15) & ~15;  // c0 + n16 <= cap
+    const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
+    mbar_arrive_expect_tx(&full[slot], 2 * cb + 2 * sb);
+    bulk_g2s(st, strm + (size_t)c0 * (D / 2), cb, &full[slot]);
+    bulk_g2s(st + Lay::kCodes, strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), cb, &full[slot]);
+    bulk_g2s(st + 2 * Lay::kCodes, strm + (size_t)cap * D + 2 * (size_t)c0, sb, &full[slot]);
+    bulk_g2s(st + 2 * Lay::kCodes + 2 * kTilePos, strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb,
+             &full[slot]);
+    return;
+  }
+  const int pi = seg_proj(k.seg);
+  mbar_arrive_expect_tx(&full[slot], (uint32_t)a.at.batch * kTileLd * 2);
+  tma_2d_box(st + kUnitBytes, maps[pi], kGroup * (k.u % a.ph[pi].n_groups), 0, &full[slot]);
+}
+
+// Has the phase before segment `seg` completed (non-blocking)?  QKV waits for
+// nothing, attention for every QKV row block, O for every attention context,
+// gate/up for O, down for gate/up.
+__device__ __forceinline__ bool seg_ready(const BlockArgs& a, int seg) {
+  if (seg == 0) return true;
+  const unsigned target = seg == 1 ? (unsigned)a.ph[0].n_rb
+                                   : (seg == 2 ? (unsigned)a.n_ctx : (unsigned)a.ph[seg - 2].n_rb);
+  return ld_acquire_gpu(&a.done[seg - 1]) >= target;
+}
+
+template <int D>
+__device__ __forceinline__ void producer(const BlockArgs& a, const CUtensorMap* const* maps, uint8_t* stages,
+                                         uint64_t* full, uint64_t* empty, int* flag) {
+  for (int m = 0; m < 4; ++m) prefetch_map(maps[m]);
   // test hook (failure path): CTA 0 issues nothing, so its consumers' bounded
   // waits run out
   const bool hold = a.pa[0].withhold && blockIdx.x == 0;
-  ProdState ps{0, !hold, global_ns() + kWaitNs};
-  w_proj<0>(a, stages, full, empty, ps);
-  w_attn<D>(a, full, empty, ps);
-  w_proj<1>(a, stages, full, empty, ps);
-  w_proj<2>(a, stages, full, empty, ps);
-  w_proj<3>(a, stages, full, empty, ps);
-  if (!ps.ok && !hold) record_timeout(a.err);
-  reinterpret_cast<volatile int*>(flag)[2] = ps.i;  // stages this producer arrived on
+  Cursor w{0, 0, 0, (int)blockIdx.x, 0, 0, 0, 0, 0};
+  Cursor x = w;
+  cursor_settle(a, w);
+  cursor_settle(a, x);
+  int wi = 0, xi = 0;
+  bool ok = !hold;
+  // the first ring's weights go out before the previous kernel has finished
+  for (; ok && w.seg < 5 && wi < a.ring; ++wi, cursor_next(a, w)) issue_weight<D>(a, w, wi, stages, full);
+  pdl_wait();  // x comes from the previous kernel
+  const unsigned long long deadline = global_ns() + kWaitNs;
+  bool x_ready = seg_ready(a, x.seg);
+  uint32_t idle = 0;
+  while (ok && (w.seg < 5 || x.seg < 5)) {
+    bool moved = false;
+    if (w.seg < 5 && stage_free(a, empty, wi)) {
+      issue_weight<D>(a, w, wi, stages, full);
+      ++wi;
+      cursor_next(a, w);
+      moved = true;
+    }
+    if (x.seg < 5 && stage_free(a, empty, xi)) {
+      if (!x_ready && seg_ready(a, x.seg)) {
+        x_ready = true;
+        fence_proxy_async_global();  // the copies read what other CTAs wrote
+      }
+      if (x_ready) {
+        issue_act<D>(a, x, xi, stages, full, maps);
+        ++xi;
+        const int seg = x.seg;
+        cursor_next(a, x);
+        if (x.seg != seg) x_ready = seg_ready(a, x.seg) && (fence_proxy_async_global(), true);
+        moved = true;
+      }
+    }
+    if (!moved && (++idle & 31u) == 0 && (global_ns() > deadline || aborted(a.err))) ok = false;
+  }
+  if (!ok && !hold) record_timeout(a.err);
+  reinterpret_cast<volatile int*>(flag)[2] = wi;  // stages each cursor arrived on
+  reinterpret_cast<volatile int*>(flag)[4] = xi;
   __threadfence_block();
   reinterpret_cast<volatile int*>(flag)[3] = 1;
-}
-
-// Wait until the phase before one (counter `cnt` of phase `prev` reached
-// `target`), then order the tensor copies after what other CTAs wrote.
-__device__ __forceinline__ bool phase_ready(const BlockArgs& a, int prev, unsigned target, ProdState& ps) {
-  if (!wait_count(&a.done[prev], target, ps.deadline, a.err)) return false;
-  fence_proxy_async_global();
-  return true;
-}
-
-// The activation producer's part of projection phase PI: one tensor copy of
-// the activation tile per unit, once the previous phase has completed.
-template <int PI>
-__device__ __forceinline__ void a_proj(const BlockArgs& a, const CUtensorMap* map, uint8_t* stages, uint64_t* full,
-                                       uint64_t* empty, ProdState& ps) {
-  const PhaseSplit sp = phase_split<PI>(a);
-  const int c = blockIdx.x;
-  if (!ps.ok || c >= sp.ne) return;
-  const int u0 = sp.lo(c), u1 = sp.lo(c + 1);
-  if (u1 <= u0) return;
-  if (PI > 0) {
-    // O waits for every context of attention, gate/up for O, down for gate/up
-    const unsigned target = PI == 1 ? (unsigned)a.n_ctx : (unsigned)a.ph[PI - 1].n_rb;
-    if (!phase_ready(a, phase_of(PI) - 1, target, ps)) {
-      ps.ok = false;
-      return;
-    }
-  }
-  const uint32_t tx = (uint32_t)a.at.batch * kTileLd * 2;
-  for (int u = u0; u < u1; ++u, ++ps.i) {
-    if (!slot_free(a, empty, ps)) {
-      ps.ok = false;
-      return;
-    }
-    const int slot = ps.i % a.ring;
-    mbar_arrive_expect_tx(&full[slot], tx);
-    tma_2d_box(stages + (size_t)slot * a.stage_bytes + kUnitBytes, map, kGroup * (u % sp.n_groups), 0, &full[slot]);
-  }
-}
-
-// The activation producer's part of the attention phase: the four bulk copies
-// of each KV tile, once every QKV row block (queries and new tokens) is done.
-template <int D>
-__device__ __forceinline__ void a_attn(const BlockArgs& a, uint8_t* stages, uint64_t* full, uint64_t* empty,
-                                       ProdState& ps) {
-  using Lay = AttnLayout<D>;
-  bool waited = false;
-  for (int j = blockIdx.x; j < a.n_ctx * a.NC && ps.ok; j += gridDim.x) {
-    const AttnItem it = attn_item(a, j);
-    if (it.t1 > it.t0 && !waited) {
-      if (!phase_ready(a, kPhQ, (unsigned)a.ph[0].n_rb, ps)) {
-        ps.ok = false;
-        return;
-      }
-      waited = true;
-    }
-    const uint8_t* strm = a.at.kv.stream(it.b, it.kvh);
-    const int cap = a.at.kv.cap;
-    for (int t = it.t0; t < it.t1; ++t, ++ps.i) {
-      if (!slot_free(a, empty, ps)) {
-        ps.ok = false;
-        return;
-      }
-      const int c0 = t * kTilePos, n16 = (min(kTilePos, it.L - c0) + 15) & ~15;  // c0 + n16 <= cap
-      const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
-      uint8_t* st = stages + (size_t)(ps.i % a.ring) * a.stage_bytes;
-      uint64_t* bar = &full[ps.i % a.ring];
-      mbar_arrive_expect_tx(bar, 2 * cb + 2 * sb);
-      bulk_g2s(st, strm + (size_t)c0 * (D / 2), cb, bar);
-      bulk_g2s(st + Lay::kCodes, strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), cb, bar);
-      bulk_g2s(st + 2 * Lay::kCodes, strm + (size_t)cap * D + 2 * (size_t)c0, sb, bar);
-      bulk_g2s(st + 2 * Lay::kCodes + 2 * kTilePos, strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb,
-               bar);
-    }
-  }
-}
-
-template <int D>
-__device__ __forceinline__ void act_producer(const BlockArgs& a, const CUtensorMap* mx, const CUtensorMap* mo,
-                                             const CUtensorMap* mh, const CUtensorMap* ma, uint8_t* stages,
-                                             uint64_t* full, uint64_t* empty, int* flag) {
-  prefetch_map(mx);
-  prefetch_map(mo);
-  prefetch_map(mh);
-  prefetch_map(ma);
-  pdl_wait();  // x comes from the previous kernel
-  ProdState ps{0, true, global_ns() + kWaitNs};
-  a_proj<0>(a, mx, stages, full, empty, ps);
-  a_attn<D>(a, stages, full, empty, ps);
-  a_proj<1>(a, mo, stages, full, empty, ps);
-  a_proj<2>(a, mh, stages, full, empty, ps);
-  a_proj<3>(a, ma, stages, full, empty, ps);
-  if (!ps.ok) record_timeout(a.err);
-  reinterpret_cast<volatile int*>(flag + 4)[0] = ps.i;
-  __threadfence_block();
-  reinterpret_cast<volatile int*>(flag + 4)[1] = 1;
 }
 
 // ------------------------------------------------------------ consumers --
@@ -347,18 +334,26 @@ __device__ __forceinline__ void attn_work(const BlockArgs& a, const AttnItem& it
   const int hq0 = it.kvh * a.at.G + it.sub * G, Gv = min(G, a.at.G - it.sub * G);
   AttnWarp<D, NTQ> aw;
   aw.init();
+  bool ok = true;
   if (it.t1 > it.t0) {
     build_qfrag<D, NTQ>(a.at.qrot + ((size_t)it.b * a.at.Hq + hq0) * D, Gv, qf, tid, kBlkCW * 32);
     consumer_sync();
     for (int t = it.t0; t < it.t1; ++t, ++cs.i) {
       if (!take_stage(a, full, cs.i, deadline)) {
-        cs.ok = false;
-        return;
+        ok = false;
+        break;
       }
       aw.tile(stages + (size_t)(cs.i % a.ring) * a.stage_bytes, min(kTilePos, it.L - t * kTilePos), qf,
               a.at.qk_scale_log2);
       give_stage(a, empty, cs.i);
     }
+  }
+  // every consumer warp learns whether some wait ran out before the next barrier
+  if (!ok) flag[1] = 1;
+  consumer_sync();
+  if (flag[1]) {
+    cs.ok = false;
+    return;
   }
   aw.finish(cm, cl, co, G, Gv);
   consumer_sync();
@@ -489,7 +484,11 @@ __device__ __forceinline__ void consumers(const BlockArgs& a, uint8_t* stages, f
   bool qready = false;
   for (int j = blockIdx.x; j < a.n_ctx * a.NC && cs.ok; j += gridDim.x) {
     if (!qready) {
-      if (!wait_count(&a.done[kPhQ], (unsigned)a.ph[0].n_rb, deadline, a.err)) {
+      // one thread waits for every QKV row block; the barrier passes its
+      // outcome (and, through its acquire, the queries) to the others
+      if (threadIdx.x == 0 && !wait_count(&a.done[kPhQ], (unsigned)a.ph[0].n_rb, deadline, a.err)) flag[1] = 1;
+      consumer_sync();
+      if (flag[1]) {
         cs.ok = false;
         break;
       }
@@ -541,10 +540,10 @@ __global__ void __launch_bounds__(kBlkThreads, kBlkPerSm<NT>)
   pdl_trigger();
 
   if (warp == kWarpP) {
-    if ((tid & 31) == 0)
-      weight_producer<D>(a, stages, full, empty, pflag);
-    else if ((tid & 31) == 1)
-      act_producer<D>(a, &map_x, &map_o, &map_h, &map_a, stages, full, empty, pflag);
+    if ((tid & 31) == 0) {
+      const CUtensorMap* maps[4] = {&map_x, &map_o, &map_h, &map_a};
+      producer<D>(a, maps, stages, full, empty, pflag);
+    }
   } else {
     consumers<NT, D>(a, stages, scratch, ss, pflag, full, empty);
   }
