@@ -74,6 +74,14 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   return v;
 }
 
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -239,14 +247,15 @@ __device__ __forceinline__ void issue_act(const BlockArgs& a, const Cursor& k, i
   tma_2d_box(st + kUnitBytes, maps[pi], kGroup * (k.u % a.ph[pi].n_groups), 0, &full[slot]);
 }
 
-// Has the phase before segment `seg` completed (non-blocking)?  QKV waits for
+// Has the phase before segment `seg` completed (non-blocking, relaxed: the
+// caller orders its copies after a fence once it has)?  QKV waits for
 // nothing, attention for every QKV row block, O for every attention context,
 // gate/up for O, down for gate/up.
 __device__ __forceinline__ bool seg_ready(const BlockArgs& a, int seg) {
   if (seg == 0) return true;
   const unsigned target = seg == 1 ? (unsigned)a.ph[0].n_rb
                                    : (seg == 2 ? (unsigned)a.n_ctx : (unsigned)a.ph[seg - 2].n_rb);
-  return ld_acquire_gpu(&a.done[seg - 1]) >= target;
+  return ld_relaxed_gpu(&a.done[seg - 1]) >= target;
 }
 
 template <int D>
@@ -266,27 +275,32 @@ __device__ __forceinline__ void producer(const BlockArgs& a, const CUtensorMap* 
   for (; ok && w.seg < 5 && wi < a.ring; ++wi, cursor_next(a, w)) issue_weight<D>(a, w, wi, stages, full);
   pdl_wait();  // x comes from the previous kernel
   const unsigned long long deadline = global_ns() + kWaitNs;
-  bool x_ready = seg_ready(a, x.seg);
-  uint32_t idle = 0;
+  bool x_ready = x.seg == 0;
+  uint32_t idle = 0, poll = 0;
   while (ok && (w.seg < 5 || x.seg < 5)) {
     bool moved = false;
-    if (w.seg < 5 && stage_free(a, empty, wi)) {
+    // weights first: every free stage gets its unit at once
+    while (w.seg < 5 && stage_free(a, empty, wi)) {
       issue_weight<D>(a, w, wi, stages, full);
       ++wi;
       cursor_next(a, w);
       moved = true;
     }
     if (x.seg < 5 && stage_free(a, empty, xi)) {
-      if (!x_ready && seg_ready(a, x.seg)) {
+      // the phase counter is polled (relaxed, every few passes) only while
+      // the activation cursor waits; once it is reached, one acquire fence
+      // orders the copies after what the other CTAs wrote
+      if (!x_ready && (poll++ & 7u) == 0 && seg_ready(a, x.seg)) {
+        fence_acquire_gpu();
+        fence_proxy_async_global();
         x_ready = true;
-        fence_proxy_async_global();  // the copies read what other CTAs wrote
       }
       if (x_ready) {
         issue_act<D>(a, x, xi, stages, full, maps);
         ++xi;
         const int seg = x.seg;
         cursor_next(a, x);
-        if (x.seg != seg) x_ready = seg_ready(a, x.seg) && (fence_proxy_async_global(), true);
+        if (x.seg != seg) x_ready = x.seg == 0;
         moved = true;
       }
     }
