@@ -202,11 +202,12 @@ futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int3
  *   a = bf16(silu(r2 W'gate h) * (r2 W'up h));  y = bf16(h + Wdown a).
  * x, y: bf16 [batch][H] (may not alias).  pos: device int32 [batch], the number
  * of tokens already cached per sequence (sequence b uses cache slot b).
- * blob: packed weights of this layer.  Batch 1..16: one persistent kernel runs
- * the whole step (all CTAs resident; it assumes no other kernel holds the GPU's
- * SMs meanwhile, else a bounded wait may report FUTR_ERR_TIMEOUT); batch 17..32,
- * or with the environment variable FUTR_PERSISTENT=0: five kernels launched
- * back to back with programmatic dependent launch.  Capturable in a CUDA graph.
+ * blob: packed weights of this layer.  Five kernels launched back to back with
+ * programmatic dependent launch.  With the environment variable
+ * FUTR_PERSISTENT=1 and batch 1..16, one persistent kernel runs the whole step
+ * instead (launched in plain stream order with all CTAs resident; it assumes no
+ * other kernel holds the GPU's SMs meanwhile, else a bounded wait may report
+ * FUTR_ERR_TIMEOUT).  Capturable in a CUDA graph.
  */
 futr_status futr_decode_block(const uint16_t* x, const void* blob, const futr_kv* kv,
                               int32_t layer, int32_t batch, const int32_t* pos, uint16_t* y,

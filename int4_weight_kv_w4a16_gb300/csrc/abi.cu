@@ -202,10 +202,11 @@ futr_status check_decode(const void* blob, const futr_kv* kv, int layer, int bat
   return FUTR_OK;
 }
 
-// Use the persistent whole-block kernel for this call?  (FUTR_PERSISTENT=0
-// selects the five kernels.)
+// Use the persistent whole-block kernel for this call?  Only when asked for
+// (FUTR_PERSISTENT=1): measured slower than the five kernels on the 8B and
+// 70B blocks, it stays an option, not the default.
 bool use_block_kernel(const Plans& P, int batch) {
-  return batch <= kBlockMaxBatch && P.blk.ok && env_int_or("FUTR_PERSISTENT", 1) != 0;
+  return batch <= kBlockMaxBatch && P.blk.ok && env_int_or("FUTR_PERSISTENT", 0) != 0;
 }
 
 // One decode step: the persistent whole-block kernel (batch <= 16), or five

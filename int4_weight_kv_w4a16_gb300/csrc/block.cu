@@ -12,8 +12,9 @@
 // waiting on another CTA; only the activation tiles (and the KV tiles of
 // attention) wait for the previous stage to complete.
 //
-// Grid: C resident CTAs per SM (all CTAs resident at once; every cross-CTA
-// wait is bounded).  A CTA has
+// Grid: C resident CTAs per SM, all resident at once: the kernel is launched
+// in plain stream order (not programmatic), after the previous kernel has
+// finished, and every cross-CTA wait is bounded.  A CTA has
 //   warps 0..3  consumers: the products of each weight unit (unit_mma, the
 //               same code as the one-projection kernels), the attention of
 //               each KV tile (AttnWarp), the split-K / split-context tails and
@@ -549,9 +550,6 @@ __global__ void __launch_bounds__(kBlkThreads, kBlkPerSm<NT>)
     fence_mbar_init();
   }
   __syncthreads();
-  // the next launch may place its CTAs as these leave: they stream their
-  // weights at once and wait (griddepcontrol.wait) for this one to finish
-  pdl_trigger();
 
   if (warp == kWarpP) {
     if ((tid & 31) == 0) {
@@ -607,11 +605,12 @@ cudaError_t launch_t(const BlockPlan& p, const BlockArgs& a, const CUtensorMap* 
   cfg.blockDim = dim3(kBlkThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  // Plain stream order, never programmatic launch: the CTAs of this grid wait
+  // on one another, so all of them must be resident together, which a grid
+  // launched early (its CTAs placed as the previous kernel's leave) does not
+  // guarantee.  It also triggers no early launch of its successor.
+  (void)pdl;
+  cfg.numAttrs = 0;
   return cudaLaunchKernelEx(&cfg, block_kernel<NT, D>, a, maps[0], maps[1], maps[2], maps[3]);
 }
 

@@ -245,23 +245,38 @@ def test_decode_wide_tensor_core_swiglu(batch):
 
 
 @pytest.mark.parametrize("batch", [1, 5, 9, 16])
-def test_decode_toy_five_kernel_path(monkeypatch, batch):
-    """Batch 1..16 runs the persistent whole-block kernel by default; the five
-    one-stage kernels (FUTR_PERSISTENT=0) stay checked at the same batches."""
-    monkeypatch.setenv("FUTR_PERSISTENT", "0")
+def test_decode_toy_whole_block_kernel(monkeypatch, batch):
+    """The persistent whole-block kernel (FUTR_PERSISTENT=1, batch 1..16) on
+    the same checks as the five-kernel path: codes, stages and the block."""
+    monkeypatch.setenv("FUTR_PERSISTENT", "1")
     r = np.random.default_rng(500 + batch)
     lengths = list(r.integers(0, 300, size=batch))
+    lengths[0] = 0
     run_case(TOY, batch, lengths, seed=batch + 50)
 
 
-def test_decode_8b_b1_five_kernel_path(monkeypatch):
-    monkeypatch.setenv("FUTR_PERSISTENT", "0")
+@pytest.mark.parametrize("name", ["g1", "g6_d128", "g12"])
+def test_decode_whole_block_kernel_query_groups(monkeypatch, name):
+    """Query groups of 1, 6 and 12 heads per kv-head: the persistent kernel
+    splits them into sub-groups of at most four heads."""
+    monkeypatch.setenv("FUTR_PERSISTENT", "1")
+    run_case(GROUP_SHAPES[name], 3, [0, 70, 129], seed=12)
+
+
+def test_decode_8b_b1_whole_block_kernel(monkeypatch):
+    monkeypatch.setenv("FUTR_PERSISTENT", "1")
     run_case(LLAMA8B, 1, [1024], seed=3)
 
 
-def test_decode_persistent_deterministic():
+def test_decode_8b_b8_whole_block_kernel(monkeypatch):
+    monkeypatch.setenv("FUTR_PERSISTENT", "1")
+    run_case(LLAMA8B, 8, [1024 - 97 * i for i in range(8)], seed=4)
+
+
+def test_decode_persistent_deterministic(monkeypatch):
     """The persistent kernel's split and merge orders are fixed: two runs of
     the same step are bit-identical (batch 1, 7 and 16)."""
+    monkeypatch.setenv("FUTR_PERSISTENT", "1")
     for batch in (1, 7, 16):
         lengths = [(53 * i + 17) % 260 for i in range(batch)]
         weights = inputs.block_weights(TOY, 21)

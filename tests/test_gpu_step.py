@@ -73,7 +73,9 @@ class Model:
                 "v_codes": vc.cpu().numpy(), "v_scales": vs.cpu().numpy().view(np.float16)}
 
 
-def test_step_toy_two_layers_end_to_end():
+@pytest.mark.parametrize("persistent", ["0", "1"], ids=["five_kernels", "whole_block"])
+def test_step_toy_two_layers_end_to_end(monkeypatch, persistent):
+    monkeypatch.setenv("FUTR_PERSISTENT", persistent)
     sh, vocab, lengths = TOY, 1024, [5, 70, 0]
     m = Model(sh, 2, vocab, max_batch=4, capacity=96)
     m.append_history(lengths)
@@ -138,3 +140,29 @@ def test_step_full_vocabulary_lm_head(batch):
     got = logits.cpu().numpy().astype(np.float64)[:, rows]
     assert_close(got, ref, "sampled logits", rel=1e-5, mx=1e-4)
     assert np.all(np.isfinite(logits.cpu().numpy()))
+
+
+def test_step_whole_block_kernel_back_to_back(monkeypatch):
+    """Steps of the 8B shape with the persistent block kernel, enqueued back to
+    back without synchronising (the block kernels follow the LM head and the
+    embedding of the step before): every step completes, and the logits equal
+    those of the five-kernel path within the block tolerance."""
+    sh, vocab, b = LLAMA8B, 4096, 1
+    m = Model(sh, 2, vocab, max_batch=b, capacity=1040, host_weights=False)
+    m.append_history([1024])
+    tokens, pos = np.array([77]), np.array([1024])
+    monkeypatch.setenv("FUTR_PERSISTENT", "0")
+    ref = m.step(tokens, pos).cpu().numpy().astype(np.float64)
+    assert futr.futr_check(m.ws, m.kv) == 0
+    monkeypatch.setenv("FUTR_PERSISTENT", "1")
+    td, pd = dev(tokens.astype(np.int32)), dev(pos.astype(np.int32))
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(6):  # enqueued without host synchronisation in between
+        o = torch.empty((b, vocab), dtype=torch.float32, device="cuda")
+        futr.futr_decode_step(td, m.embedding, vocab, m.blobs, m.kv, b, pd, m.g_final, m.lm_head, o, m.ws)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert futr.futr_check(m.ws, m.kv) == 0
+    for o in outs:
+        assert_close(o.cpu().numpy().astype(np.float64), ref, "logits, whole-block kernel", rel=2e-3)
