@@ -44,6 +44,7 @@ typedef int32_t futr_status;
 #define FUTR_ERR_OUT_OF_RANGE  4  /* device: pos[b] outside [0, capacity)             */
 #define FUTR_ERR_TIMEOUT       5  /* device: a bounded wait ran out                   */
 #define FUTR_ERR_BAD_BLOB      6  /* device or host: weight blob header mismatch      */
+#define FUTR_ERR_NOT_PD        7  /* GPTQ: a dampened Hessian is not positive definite */
 
 /* Shape of one decoder block. */
 typedef struct futr_shape {
@@ -135,6 +136,50 @@ futr_status futr_pack_weights(const futr_shape* shape,
                               const float* wo, const float* wgate, const float* wup,
                               const float* wdown, const float* g_attn, const float* g_mlp,
                               void* blob, size_t blob_bytes, void* stream);
+
+/* Bytes of device scratch futr_pack_weights_gptq needs for `shape`: two
+ * float64 K x K matrices for the largest input width K of the block (the
+ * intermediate size), a float64 copy of the largest projection, and its codes. */
+futr_status futr_gptq_scratch_size(const futr_shape* shape, size_t* bytes);
+
+/*
+ * GPTQ packer: the same blob as futr_pack_weights (same header, layout, scale
+ * rule s = fp16(max|w| / 7) and code range), with the codes chosen by GPTQ.
+ * The abstract quantizes the decode weights with GPTQ in the round-to-nearest
+ * INT4 format; the explainer's accuracy section describes it as using
+ * calibration data and approximate second-order information.  The steps are
+ * those of the published GPTQ algorithm (Frantar et al., 2022), columns in
+ * natural order, no activation reordering:
+ *   H' = H with every dead input (H_jj = 0) set to H_jj = 1 and its weight
+ *        column to 0, then H' += damp * mean(diag H') * I;
+ *   U  = upper Cholesky factor of H'^-1 (H'^-1 = U^T U);
+ *   for j = 0..K-1 on a float64 copy of W' = fp32(W diag(g)): at the first
+ *   input of each 128-group the group's scales are taken from its current
+ *   weights (rounded to fp32); c_j = clamp(rint(fp32(w_j) / s), -8, 7);
+ *   e = (w_j - c_j s) / U_jj; W[:, j+1:] -= e U[j, j+1:].
+ * Everything runs in float64 on the device (blocked Cholesky and triangular
+ * inverse, the sweep in 128-column blocks with the trailing update as a GEMM);
+ * the float64 additions come in another order than the column-by-column sweep.
+ *
+ * Hessians (float64 device, symmetric, [K, K] for the projection's input
+ * width K): h_attn [H, H] of the normalized block input (QKV), h_o
+ * [Hq*d, Hq*d] of the attention output (O), h_mlp [H, H] of the normalized
+ * residual (gate and up), h_down [I, I] of the SwiGLU output (down); a
+ * calibration set X [n, K] gives H = (2/n) X^T X.  damp > 0 (0.01 is usual).
+ * scratch: futr_gptq_scratch_size bytes, 256-byte aligned; its contents are
+ * undefined afterwards.  Other arguments as for futr_pack_weights.
+ * Synchronous: returns after `stream` has finished.  FUTR_ERR_NOT_PD when a
+ * dampened Hessian has a non-positive Cholesky pivot (the blob is then not
+ * usable).
+ */
+futr_status futr_pack_weights_gptq(const futr_shape* shape,
+                                   const float* wq, const float* wk, const float* wv,
+                                   const float* wo, const float* wgate, const float* wup,
+                                   const float* wdown, const float* g_attn, const float* g_mlp,
+                                   const double* h_attn, const double* h_o, const double* h_mlp,
+                                   const double* h_down, double damp,
+                                   void* scratch, size_t scratch_bytes,
+                                   void* blob, size_t blob_bytes, void* stream);
 
 /*
  * Canonical view of one packed projection (for verification): codes int8

@@ -357,6 +357,7 @@ const char* futr_status_string(futr_status s) {
     case FUTR_ERR_OUT_OF_RANGE: return "position outside the KV cache";
     case FUTR_ERR_TIMEOUT: return "device wait timed out";
     case FUTR_ERR_BAD_BLOB: return "weight blob header mismatch";
+    case FUTR_ERR_NOT_PD: return "dampened Hessian not positive definite";
     default: return "unknown status";
   }
 }
@@ -381,6 +382,36 @@ futr_status futr_pack_weights(const futr_shape* shape, const float* wq, const fl
     return FUTR_ERR_INVALID_ARG;
   return cuda_status(launch_pack(*shape, wq, wk, wv, wo, wgate, wup, wdown, g_attn, g_mlp,
                                  reinterpret_cast<uint8_t*>(blob), as_stream(stream)));
+}
+
+futr_status futr_gptq_scratch_size(const futr_shape* shape, size_t* bytes) {
+  if (!bytes) return FUTR_ERR_INVALID_ARG;
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  *bytes = gptq_scratch_bytes(*shape);
+  return FUTR_OK;
+}
+
+futr_status futr_pack_weights_gptq(const futr_shape* shape, const float* wq, const float* wk, const float* wv,
+                                   const float* wo, const float* wgate, const float* wup, const float* wdown,
+                                   const float* g_attn, const float* g_mlp, const double* h_attn,
+                                   const double* h_o, const double* h_mlp, const double* h_down, double damp,
+                                   void* scratch, size_t scratch_bytes, void* blob, size_t blob_bytes,
+                                   void* stream) {
+  if (!shape_ok(shape)) return FUTR_ERR_UNSUPPORTED;
+  if (!wq || !wk || !wv || !wo || !wgate || !wup || !wdown || !g_attn || !g_mlp || !blob || !h_attn || !h_o ||
+      !h_mlp || !h_down || !scratch)
+    return FUTR_ERR_INVALID_ARG;
+  if (!(damp > 0.0) || !std::isfinite(damp)) return FUTR_ERR_INVALID_ARG;
+  if (blob_bytes < blob_sections(*shape).total || (reinterpret_cast<uintptr_t>(blob) & 255))
+    return FUTR_ERR_INVALID_ARG;
+  if (scratch_bytes < gptq_scratch_bytes(*shape) || (reinterpret_cast<uintptr_t>(scratch) & 255))
+    return FUTR_ERR_INVALID_ARG;
+  int bad = 0;
+  const futr_status st = cuda_status(launch_pack_gptq(*shape, wq, wk, wv, wo, wgate, wup, wdown, g_attn, g_mlp,
+                                                      h_attn, h_o, h_mlp, h_down, damp, scratch,
+                                                      reinterpret_cast<uint8_t*>(blob), &bad, as_stream(stream)));
+  if (st != FUTR_OK) return st;
+  return bad ? FUTR_ERR_NOT_PD : FUTR_OK;
 }
 
 futr_status futr_unpack_weights(const futr_shape* shape, const void* blob, int32_t which, int8_t* codes,

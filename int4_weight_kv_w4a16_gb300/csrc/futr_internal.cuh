@@ -467,6 +467,13 @@ cudaError_t launch_pack(const futr_shape& s, const float* wq, const float* wk, c
                         const float* ga, const float* gm, uint8_t* blob, cudaStream_t st);
 cudaError_t launch_unpack(const futr_shape& s, const uint8_t* blob, int which, int8_t* codes,
                           uint16_t* scales, cudaStream_t st);
+size_t gptq_scratch_bytes(const futr_shape& s);
+// Synchronizes st; *bad_host = 1 when a dampened Hessian was not positive definite.
+cudaError_t launch_pack_gptq(const futr_shape& s, const float* wq, const float* wk, const float* wv,
+                             const float* wo, const float* wg, const float* wu, const float* wd, const float* ga,
+                             const float* gm, const double* h_attn, const double* h_o, const double* h_mlp,
+                             const double* h_down, double damp, void* scratch, uint8_t* blob, int* bad_host,
+                             cudaStream_t st);
 cudaError_t launch_rope_table(float2* table, int cap, int d, float theta, cudaStream_t st);
 cudaError_t launch_kv_append(const futr_kv& kv, int layer, int seq0, int batch, const int* pos,
                              int n_tok, const uint16_t* k, const uint16_t* v, int* err,

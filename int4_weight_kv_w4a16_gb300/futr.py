@@ -22,6 +22,7 @@ FUTR_ERR_CUDA = 3
 FUTR_ERR_OUT_OF_RANGE = 4
 FUTR_ERR_TIMEOUT = 5
 FUTR_ERR_BAD_BLOB = 6
+FUTR_ERR_NOT_PD = 7
 
 FUTR_PROJ_QKV, FUTR_PROJ_O, FUTR_PROJ_GATE, FUTR_PROJ_UP, FUTR_PROJ_DOWN = range(5)
 
@@ -63,6 +64,9 @@ _SIGS = {
     "futr_version": (I32, []),
     "futr_weights_size": (I32, [C.POINTER(futr_shape), C.POINTER(C.c_size_t)]),
     "futr_pack_weights": (I32, [C.POINTER(futr_shape)] + [P] * 10 + [C.c_size_t, P]),
+    "futr_gptq_scratch_size": (I32, [C.POINTER(futr_shape), C.POINTER(C.c_size_t)]),
+    "futr_pack_weights_gptq": (I32, [C.POINTER(futr_shape)] + [P] * 13 + [C.c_double, P, C.c_size_t, P,
+                                                                          C.c_size_t, P]),
     "futr_unpack_weights": (I32, [C.POINTER(futr_shape), P, I32, P, P, P]),
     "futr_kv_size": (I32, [C.POINTER(futr_shape), I32, I32, I32, C.POINTER(C.c_size_t)]),
     "futr_kv_init": (I32, [C.POINTER(futr_shape), I32, I32, I32, P, C.c_size_t, C.POINTER(futr_kv), P]),
@@ -146,6 +150,22 @@ def futr_pack_weights(shape, wq, wk, wv, wo, wgate, wup, wdown, g_attn, g_mlp, b
     _ok(lib().futr_pack_weights(C.byref(shape), *[_ptr(t) for t in (wq, wk, wv, wo, wgate, wup, wdown,
                                                                     g_attn, g_mlp, blob)],
                                 blob.numel() * blob.element_size(), _stream(stream)), "futr_pack_weights")
+
+
+def futr_gptq_scratch_size(shape) -> int:
+    n = C.c_size_t()
+    _ok(lib().futr_gptq_scratch_size(C.byref(shape), C.byref(n)), "futr_gptq_scratch_size")
+    return n.value
+
+
+def futr_pack_weights_gptq(shape, wq, wk, wv, wo, wgate, wup, wdown, g_attn, g_mlp, h_attn, h_o, h_mlp, h_down,
+                           damp, scratch, blob, stream=None):
+    _ok(lib().futr_pack_weights_gptq(C.byref(shape), *[_ptr(t) for t in (wq, wk, wv, wo, wgate, wup, wdown,
+                                                                         g_attn, g_mlp, h_attn, h_o, h_mlp,
+                                                                         h_down)],
+                                     float(damp), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                     _ptr(blob), blob.numel() * blob.element_size(), _stream(stream)),
+        "futr_pack_weights_gptq")
 
 
 def futr_unpack_weights(shape, blob, which, codes, scales, stream=None):

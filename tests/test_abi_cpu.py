@@ -130,3 +130,39 @@ def test_no_alloc_rejects_zeroed_cache_descriptor(L):
     assert L.futr_decode_block_noalloc(C.addressof(buf), C.addressof(buf), C.byref(kv), 0, 1, C.addressof(pos),
                                        C.addressof(buf) + 256, None) == futr.FUTR_ERR_INVALID_ARG
     assert L.futr_decode_block_noalloc(None, None, None, 0, 1, None, None, None) == futr.FUTR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("shape", [TOY, LLAMA8B, LLAMA70B], ids=["toy", "8b", "70b"])
+def test_gptq_scratch_size_covers_its_buffers(L, shape):
+    """Two float64 K x K matrices for the widest projection input, a float64
+    copy of the largest single projection, its block errors and its codes."""
+    n = futr.futr_gptq_scratch_size(futr.make_shape(shape))
+    kmax = max(shape.hidden, shape.q_rows, shape.inter)
+    largest = max(shape.qkv_rows * shape.hidden, shape.hidden * shape.q_rows, shape.inter * shape.hidden,
+                  shape.hidden * shape.inter)
+    assert n >= 2 * 8 * kmax * kmax + 8 * largest + 2 * largest
+
+
+def test_gptq_arguments_rejected_without_gpu(L):
+    sh = futr.make_shape(TOY)
+    fake = C.c_void_p(1 << 20)  # never dereferenced: every check below is on the host
+    blob_n = futr.futr_weights_size(sh)
+    scr_n = futr.futr_gptq_scratch_size(sh)
+    ptrs = [fake] * 13
+
+    def call(damp=0.01, scr=fake, scr_n=scr_n, blob=fake, blob_n=blob_n, ptrs=ptrs):
+        return L.futr_pack_weights_gptq(C.byref(sh), *ptrs, C.c_double(damp), scr, scr_n, blob, blob_n, None)
+
+    assert call(damp=0.0) == futr.FUTR_ERR_INVALID_ARG
+    assert call(damp=-1.0) == futr.FUTR_ERR_INVALID_ARG
+    assert call(damp=float("nan")) == futr.FUTR_ERR_INVALID_ARG
+    assert call(scr_n=scr_n - 1) == futr.FUTR_ERR_INVALID_ARG
+    assert call(scr=C.c_void_p((1 << 20) + 16)) == futr.FUTR_ERR_INVALID_ARG
+    assert call(blob_n=blob_n - 1) == futr.FUTR_ERR_INVALID_ARG
+    assert call(scr=None) == futr.FUTR_ERR_INVALID_ARG
+    assert call(ptrs=[fake] * 12 + [None]) == futr.FUTR_ERR_INVALID_ARG
+    import dataclasses
+    bad = futr.make_shape(dataclasses.replace(TOY, head_dim=96))
+    assert L.futr_pack_weights_gptq(C.byref(bad), *ptrs, C.c_double(0.01), fake, scr_n, fake, blob_n, None) == \
+        futr.FUTR_ERR_UNSUPPORTED
+    assert "positive definite" in futr.futr_status_string(futr.FUTR_ERR_NOT_PD)

@@ -145,16 +145,26 @@ def test_step_full_vocabulary_lm_head(batch):
 def test_step_whole_block_kernel_back_to_back(monkeypatch):
     """Steps of the 8B shape with the persistent block kernel, enqueued back to
     back without synchronising (the block kernels follow the LM head and the
-    embedding of the step before): every step completes, and the logits equal
-    those of the five-kernel path within the block tolerance."""
+    embedding of the step before): every step completes and gives, bit for
+    bit, the logits of a step run alone (the kernel is deterministic, so a race
+    between consecutive launches would show here).
+
+    Against the five-kernel path only a loose bound holds: the two paths sum
+    in different orders, a few bf16 roundings of h land on the other side of a
+    boundary, and the gate/up projections spread each such step over every
+    SwiGLU output (about a sixth of them then round differently).  Each path
+    is held to the oracle block by block by the parity tests; here the two
+    differ by 2.7e-3 relative after two layers."""
     sh, vocab, b = LLAMA8B, 4096, 1
     m = Model(sh, 2, vocab, max_batch=b, capacity=1040, host_weights=False)
     m.append_history([1024])
     tokens, pos = np.array([77]), np.array([1024])
     monkeypatch.setenv("FUTR_PERSISTENT", "0")
-    ref = m.step(tokens, pos).cpu().numpy().astype(np.float64)
+    five = m.step(tokens, pos).cpu().numpy().astype(np.float64)
     assert futr.futr_check(m.ws, m.kv) == 0
     monkeypatch.setenv("FUTR_PERSISTENT", "1")
+    alone = m.step(tokens, pos).cpu().numpy()
+    assert futr.futr_check(m.ws, m.kv) == 0
     td, pd = dev(tokens.astype(np.int32)), dev(pos.astype(np.int32))
     torch.cuda.synchronize()
     outs = []
@@ -165,4 +175,5 @@ def test_step_whole_block_kernel_back_to_back(monkeypatch):
     torch.cuda.synchronize()
     assert futr.futr_check(m.ws, m.kv) == 0
     for o in outs:
-        assert_close(o.cpu().numpy().astype(np.float64), ref, "logits, whole-block kernel", rel=2e-3)
+        np.testing.assert_array_equal(o.cpu().numpy(), alone)
+    assert_close(alone.astype(np.float64), five, "logits, whole-block vs five kernels", rel=1e-2)
