@@ -45,6 +45,8 @@ typedef int32_t futr_status;
 #define FUTR_ERR_TIMEOUT       5  /* device: a bounded wait ran out                   */
 #define FUTR_ERR_BAD_BLOB      6  /* device or host: weight blob header mismatch      */
 #define FUTR_ERR_NOT_PD        7  /* GPTQ: a dampened Hessian is not positive definite */
+#define FUTR_ERR_CORRUPT       8  /* device: guard words after a region overwritten    */
+#define FUTR_ERR_BOUNDS        9  /* device, debug build: an index failed its check    */
 
 /* Shape of one decoder block. */
 typedef struct futr_shape {
@@ -195,7 +197,8 @@ futr_status futr_kv_size(const futr_shape* shape, int32_t n_layers, int32_t max_
                          int32_t capacity, size_t* bytes);
 
 /* Zero `kv_mem`, write the RoPE cos/sin table (float64 evaluation rounded to
- * fp32) and fill the host descriptor `kv`.  Asynchronous on `stream`. */
+ * fp32) and the guard words after each region (see futr_check), and fill the
+ * host descriptor `kv`.  Asynchronous on `stream`. */
 futr_status futr_kv_init(const futr_shape* shape, int32_t n_layers, int32_t max_batch,
                          int32_t capacity, void* kv_mem, size_t kv_bytes, futr_kv* kv,
                          void* stream);
@@ -230,8 +233,9 @@ futr_status futr_kv_read(const futr_kv* kv, int32_t layer, int32_t seq, int32_t 
 futr_status futr_workspace_size(const futr_shape* shape, int32_t max_batch, int32_t capacity,
                                 size_t* bytes);
 
-/* Zero the workspace (its counters must start at 0) and fill `ws`.  The
- * current CUDA device must be the one the workspace lives on. */
+/* Zero the workspace (its counters must start at 0), write the guard words
+ * after each region (see futr_check) and fill `ws`.  The current CUDA device
+ * must be the one the workspace lives on. */
 futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int32_t capacity,
                                 void* ws_mem, size_t ws_bytes, futr_ws* ws, void* stream);
 
@@ -330,9 +334,13 @@ futr_status futr_decode_step(const int32_t* tokens, const uint16_t* embedding, i
                              const uint16_t* lm_head, float* logits, const futr_ws* ws,
                              void* stream);
 
-/* Synchronize `stream`, then return (and clear) the first nonzero device error
- * word of the workspace `ws` and of the cache `kv` (either may be NULL), or
- * FUTR_ERR_CUDA if a CUDA error is pending. */
+/* Compare the guard words of `ws` and `kv` with their pattern (every region of
+ * a workspace and of a cache is followed by 256 guard bytes that
+ * futr_workspace_init / futr_kv_init fill and no kernel writes; an overwritten
+ * guard sets FUTR_ERR_CORRUPT, and stays overwritten until the buffer is
+ * initialised again), synchronize `stream`, then return (and clear) the first
+ * nonzero device error word of the workspace `ws` and of the cache `kv` (either
+ * may be NULL), or FUTR_ERR_CUDA if a CUDA error is pending. */
 futr_status futr_check(const futr_ws* ws, const futr_kv* kv, void* stream);
 
 #ifdef __cplusplus

@@ -10,6 +10,8 @@
 #include <string>
 #include <tuple>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "futr_internal.cuh"
 #include "proj.cuh"
 
@@ -20,6 +22,32 @@ namespace {
 constexpr int kVersion = 10000;
 
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+// Per-stage NVTX ranges (FUTR_NVTX=1 in the environment, read once): a
+// host-side range named for the stage around each kernel launch, for timeline
+// tools.  Off by default.
+bool nvtx_on();
+struct Range {
+  const bool on;
+  explicit Range(const char* name) : on(nvtx_on()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~Range() {
+    if (on) nvtxRangePop();
+  }
+};
+
+// Guard words: every region of a workspace and of a cache is followed by
+// kGuardBytes of a fixed pattern (written at init, never by a kernel), so the
+// guard of a region is the kGuardBytes just before the next region's start (the
+// buffer's end for the last one).  futr_check compares them with the pattern:
+// a kernel that wrote past the end of a region shows up as FUTR_ERR_CORRUPT.
+constexpr uint64_t kGuardBytes = 256;
+constexpr unsigned char kGuardByte = 0xA5;
+constexpr uint32_t kGuardWord = 0xA5A5A5A5u;
+constexpr int kMaxGuards = 16;
+// the next region's start after one of `size` bytes at `off`
+inline uint64_t after(uint64_t off, uint64_t size) { return align256(off + size) + kGuardBytes; }
 
 bool shape_ok(const futr_shape* s) {
   if (!s) return false;
@@ -49,6 +77,11 @@ int current_sm_count() {
 int env_int(const char* name) {
   const char* v = std::getenv(name);
   return v ? std::atoi(v) : 0;
+}
+
+bool nvtx_on() {
+  static const bool on = env_int("FUTR_NVTX") == 1;
+  return on;
 }
 
 int round16(int c) { return (c + 15) & ~15; }
@@ -115,14 +148,14 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
   const uint64_t B = (uint64_t)max_batch;
   const uint64_t qd = (uint64_t)s.n_q_heads * s.head_dim;
   uint64_t off = 0;
-  L.err = off; off = align256(off + 16);
-  L.qrot = off; off = align256(off + B * qd * 4);
-  L.o = off; off = align256(off + B * qd * 2);
-  L.h = off; off = align256(off + B * s.hidden * 2);
-  L.a = off; off = align256(off + B * s.inter * 2);
-  L.xin = off; off = align256(off + B * s.hidden * 2);
-  L.yout = off; off = align256(off + B * s.hidden * 2);
-  L.pos = off; off = align256(off + B * 4);
+  L.err = off; off = after(off, 16);
+  L.qrot = off; off = after(off, B * qd * 4);
+  L.o = off; off = after(off, B * qd * 2);
+  L.h = off; off = after(off, B * s.hidden * 2);
+  L.a = off; off = after(off, B * s.inter * 2);
+  L.xin = off; off = after(off, B * s.hidden * 2);
+  L.yout = off; off = after(off, B * s.hidden * 2);
+  L.pos = off; off = after(off, B * 4);
   // split records: the largest any plan of a batch up to max_batch can use
   // (each projection's split cap, independent of occupancy answers and of
   // forced split counts)
@@ -151,14 +184,14 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
       }
     }
   }
-  L.part = off; L.part_bytes = part * 4; off = align256(off + L.part_bytes);
-  L.apart = off; L.apart_bytes = apart * 4; off = align256(off + L.apart_bytes);
+  L.part = off; L.part_bytes = part * 4; off = after(off, L.part_bytes);
+  L.apart = off; L.apart_bytes = apart * 4; off = after(off, L.apart_bytes);
   // split-K arrival counters, one per row block of each projection; then the
   // persistent kernel's context counters and its six phase counters
   uint64_t cnt = 0;
   for (int i = 0; i < 4; ++i) cnt += sec.rows[i] / kRowsPerBlock;
   cnt += n_ctx_max + 6;
-  L.cnt = off; L.cnt_words = cnt; off = align256(off + cnt * 4);
+  L.cnt = off; L.cnt_words = cnt; off = after(off, cnt * 4);
   L.total = off;
   return L;
 }
@@ -170,12 +203,54 @@ struct KvLayout {
 KvLayout kv_layout(const futr_shape& s, int n_layers, int max_batch, int cap16) {
   KvLayout L{};
   L.stream_bytes = kv_stream_bytes(cap16, s.head_dim);
-  uint64_t off = align256((uint64_t)n_layers * max_batch * s.n_kv_heads * L.stream_bytes);
+  uint64_t off = after(0, (uint64_t)n_layers * max_batch * s.n_kv_heads * L.stream_bytes);
   L.rope = off;
-  off = align256(off + (uint64_t)cap16 * (s.head_dim / 2) * 8);
+  off = after(off, (uint64_t)cap16 * (s.head_dim / 2) * 8);
   L.err = off;
-  L.total = align256(off + 16);
+  L.total = after(off, 16);
   return L;
+}
+
+// Guard offsets of a workspace / cache described by `d` (see kGuardBytes).
+int ws_guards(const futr_ws& d, uint64_t* g) {
+  const uint64_t starts[] = {d.off_err, d.off_qrot, d.off_o, d.off_h, d.off_a, d.off_xin, d.off_yout,
+                             d.off_pos, d.off_part, d.off_apart, d.off_cnt, d.bytes};
+  int n = 0;
+  for (size_t i = 1; i < sizeof(starts) / sizeof(starts[0]); ++i) g[n++] = starts[i] - kGuardBytes;
+  return n;
+}
+
+int kv_guards(const futr_kv& d, uint64_t* g) {
+  g[0] = d.rope_offset - kGuardBytes;
+  g[1] = d.err_offset - kGuardBytes;
+  g[2] = d.bytes - kGuardBytes;
+  return 3;
+}
+
+cudaError_t fill_guards(void* base, const uint64_t* g, int n, cudaStream_t st) {
+  for (int i = 0; i < n; ++i) {
+    const cudaError_t e = cudaMemsetAsync(reinterpret_cast<uint8_t*>(base) + g[i], kGuardByte, kGuardBytes, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+struct GuardList {
+  uint64_t off[kMaxGuards];
+};
+
+// One CTA per guard, one thread per word: a word off the pattern sets
+// FUTR_ERR_CORRUPT in `err`.
+__global__ void guard_check_kernel(const uint8_t* base, const GuardList g, int* err) {
+  const uint32_t w = reinterpret_cast<const uint32_t*>(base + g.off[blockIdx.x])[threadIdx.x];
+  if (w != kGuardWord) atomicCAS(err, 0, FUTR_ERR_CORRUPT);
+}
+
+cudaError_t check_guards(void* base, const uint64_t* g, int n, int* err, cudaStream_t st) {
+  GuardList l{};
+  for (int i = 0; i < n; ++i) l.off[i] = g[i];
+  guard_check_kernel<<<n, (unsigned)(kGuardBytes / 4), 0, st>>>(reinterpret_cast<const uint8_t*>(base), l, err);
+  return cudaGetLastError();
 }
 
 bool kv_ok(const futr_kv* kv) { return kv && kv->magic == kKvMagic && kv->base; }
@@ -255,6 +330,15 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     A.resid = resid[i];
     A.out = outs[i];
     A.out_ld = out_ld[i];
+    A.n_rb = sec.rows[i] / kRowsPerBlock;
+    A.part_cap = ws->part_bytes / 4;
+    A.out_cap = (size_t)batch * out_ld[i];
+#ifdef FUTR_DEBUG
+    // FUTR_TEST_SHRINK_PART=1 (debug build, tests of the bounds checks only):
+    // the split records are checked against a region of one float, so the
+    // first record write fails its check and is skipped
+    if (env_int("FUTR_TEST_SHRINK_PART") == 1) A.part_cap = 1;
+#endif
     if (i == 0) {
       A.blob_magic = reinterpret_cast<const uint64_t*>(blob);
       A.qrot = qrot;
@@ -321,6 +405,7 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     CUtensorMap maps[4];
     for (int i = 0; i < 4; ++i)
       if (!make_proj_tile_map(&maps[i], xin[i], batch, sec.cols[i], batch)) return FUTR_ERR_CUDA;
+    Range r("futr.block");
     return cuda_status(launch_block(bp, B, maps, st, pdl));
   }
 
@@ -328,14 +413,19 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     if (P.proj[i].S > 1 && P.proj[i].part_floats * 4 > ws->part_bytes) return FUTR_ERR_INVALID_ARG;
   if (P.attn.part_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
+  static const char* const names[4] = {"futr.qkv", "futr.o", "futr.gate_up", "futr.down"};
   cudaError_t e;
   for (int i = 0; i < 4; ++i) {
     if (events) cudaEventRecord(events[i == 0 ? 0 : i + 1], st);
-    e = launch_projection(epi[i], P.proj[i], PA[i], st, pdl);
+    {
+      Range r(names[i]);
+      e = launch_projection(epi[i], P.proj[i], PA[i], st, pdl);
+    }
     if (e != cudaSuccess) return FUTR_ERR_CUDA;
     if (i == 0) {
       // S3: attention
       if (events) cudaEventRecord(events[1], st);
+      Range r("futr.attention");
       e = launch_attention(P.attn, AT, s.head_dim, st, pdl);
       if (e != cudaSuccess) return FUTR_ERR_CUDA;
     }
@@ -358,6 +448,8 @@ const char* futr_status_string(futr_status s) {
     case FUTR_ERR_TIMEOUT: return "device wait timed out";
     case FUTR_ERR_BAD_BLOB: return "weight blob header mismatch";
     case FUTR_ERR_NOT_PD: return "dampened Hessian not positive definite";
+    case FUTR_ERR_CORRUPT: return "guard words after a workspace or cache region overwritten";
+    case FUTR_ERR_BOUNDS: return "device bounds check failed (debug build)";
     default: return "unknown status";
   }
 }
@@ -458,6 +550,8 @@ futr_status futr_kv_init(const futr_shape* shape, int32_t n_layers, int32_t max_
   d.rope_offset = L.rope;
   d.err_offset = L.err;
   d.magic = kKvMagic;
+  uint64_t g[kMaxGuards];
+  if (fill_guards(kv_mem, g, kv_guards(d, g), st) != cudaSuccess) return FUTR_ERR_CUDA;
   *kv = d;
   return FUTR_OK;
 }
@@ -527,6 +621,8 @@ futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int3
   d.off_cnt = L.cnt;
   d.cnt_words = L.cnt_words;
   d.magic = kWsMagic;
+  uint64_t g[kMaxGuards];
+  if (fill_guards(ws_mem, g, ws_guards(d, g), as_stream(stream)) != cudaSuccess) return FUTR_ERR_CUDA;
   *ws = d;
   return FUTR_OK;
 }
@@ -602,6 +698,7 @@ futr_status futr_decode_step(const int32_t* tokens, const uint16_t* embedding, i
   uint16_t* buf[2] = {at<uint16_t>(base, ws->off_xin), at<uint16_t>(base, ws->off_yout)};
   uint16_t* xg = at<uint16_t>(base, ws->off_h);
   float* r = at<float>(base, ws->off_qrot);
+  Range range("futr.step");
   if (launch_embed(tokens, embedding, vocab, s.hidden, batch, buf[0], err, st, true) != cudaSuccess)
     return FUTR_ERR_CUDA;
   for (int l = 0; l < n_layers; ++l) {
@@ -615,6 +712,12 @@ futr_status futr_decode_step(const int32_t* tokens, const uint16_t* embedding, i
 
 futr_status futr_check(const futr_ws* ws, const futr_kv* kv, void* stream) {
   cudaStream_t s = as_stream(stream);
+  // the guard words after every region (a write past a region's end)
+  uint64_t g[kMaxGuards];
+  if (ws_ok(ws) && check_guards(ws->base, g, ws_guards(*ws, g), at<int>(ws->base, ws->off_err), s) != cudaSuccess)
+    return FUTR_ERR_CUDA;
+  if (kv_ok(kv) && check_guards(kv->base, g, kv_guards(*kv, g), at<int>(kv->base, kv->err_offset), s) != cudaSuccess)
+    return FUTR_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return FUTR_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return FUTR_ERR_CUDA;
   futr_status result = FUTR_OK;

@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
       auto issue = [&](int slot, int i) {
         const int c0 = (tile0 + i) * kTilePos;
         const int n16 = (min(kTilePos, L - c0) + 15) & ~15;  // c0 + n16 <= round16(L) <= cap
+        if (!FUTR_DCHECK(c0 >= 0 && c0 + n16 <= cap, a.err)) return;  // debug build
         const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
         uint8_t* st = stages + (size_t)slot * Lay::kStage;
         mbar_arrive_expect_tx(&full[slot], 2 * cb + 2 * sb);

@@ -331,6 +331,25 @@ __device__ __forceinline__ void record_timeout(int* err) {
   atomicExch(err + 1, 1);
 }
 
+// Debug build (compiled with -DFUTR_DEBUG): FUTR_DCHECK(cond, err) tests an
+// index or range before a global access; a failed check records
+// FUTR_ERR_BOUNDS with the source line (error word 2), raises the abort word
+// so every bounded wait of the launch ends, and is false, so the caller skips
+// the access.  In the release build it is the constant true and the condition
+// is not evaluated.
+__device__ __noinline__ inline bool dcheck_fail(int* err, int line) {
+  if (err) {
+    if (atomicCAS(err, 0, FUTR_ERR_BOUNDS) == 0) err[2] = line;
+    atomicExch(err + 1, 1);
+  }
+  return false;
+}
+#ifdef FUTR_DEBUG
+#define FUTR_DCHECK(cond, err) ((cond) ? true : ::futr::dcheck_fail((err), __LINE__))
+#else
+#define FUTR_DCHECK(cond, err) true
+#endif
+
 // ------------------------------------------------- rotation + quantizer --
 // One warp holds a d-vector (d = 32*J, element i = lane + 32*j in v[j]).
 // fp32 fast Walsh-Hadamard transform in blocks of nh (power of two <= d):

@@ -90,7 +90,8 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       const uint32_t tx = kUnitBytes + (kRow1 ? kGroup * 2 : (uint32_t)a.batch * kTileLd * 2);
-      const bool hold = a.withhold && blockIdx.x == 0;  // test hook: no copy is issued
+      // test hook: no copy is issued; debug build: the units lie in the section
+      const bool hold = (a.withhold && blockIdx.x == 0) || !FUTR_DCHECK(rb < a.n_rb && g1 <= a.n_groups, a.err);
       const int pre = hold ? 0 : (ng < R ? ng : R);
       if (!kRow1) prefetch_map(xmap);
       for (int i = 0; i < pre; ++i) {

@@ -28,6 +28,10 @@ struct ProjArgs {
   unsigned* cnt;                 // arrival counters [n_rb]
   int* err;
   float eps;
+  // extents the debug build checks accesses against: floats of `part`, rows
+  // blocks of the section, elements of `out` (RESID / SWIGLU)
+  size_t part_cap, out_cap;
+  int n_rb;
   // failure injection for tests: when 1, CTA 0 issues no copy at all, so its
   // consumers' bounded waits run out (0 in every normal call)
   int withhold;

@@ -89,6 +89,7 @@ __device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, in
     }
   }
   warp_fwht<J>(v, a.nh, a.had_c);
+  if (!FUTR_DCHECK(n < a.batch && hg < a.Hq + 2 * a.Hkv, a.err)) return;
   if (is_q) {
     float* q = a.qrot + ((size_t)n * a.Hq + hg) * d;
 #pragma unroll
@@ -194,6 +195,12 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
     record_timeout(a.err);
     flag[1] = 1;
   }
+  // debug build: this CTA's split record and row block lie inside their regions
+  if (tid == 0 && S > 1 &&
+      !FUTR_DCHECK(rb < a.n_rb && slot < a.part_stride &&
+                       ((size_t)rb * a.part_stride + a.part_stride) * a.rec_floats <= a.part_cap,
+                   a.err))
+    flag[1] = 1;
 
   // ------------------------------------------------------------ epilogue --
   consumer_sync();  // every warp is done with its accumulators (and, in a one-shot kernel, the ring)
@@ -319,7 +326,8 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
     for (int n = 0; n < NT * 8; ++n)
       if (n < a.batch) {
         const size_t o = (size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + tid;
-        a.out[o] = __float2bfloat16_rn(__bfloat162float(rres[n]) + red[n * kRedLd + tid]);
+        if (FUTR_DCHECK(o < a.out_cap, a.err))
+          a.out[o] = __float2bfloat16_rn(__bfloat162float(rres[n]) + red[n * kRedLd + tid]);
       }
   } else if (EPI == kEpiSwiglu) {
     for (int e = tid; e < a.batch * 64; e += kCW * 32) {
@@ -328,7 +336,8 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
       const float g = rn * red[n * kRedLd + r];
       const float u = rn * red[n * kRedLd + 64 + r];
       const float sg = __fdiv_rn(g, 1.0f + expf(-g));
-      a.out[(size_t)n * a.out_ld + (size_t)rb * 64 + r] = __float2bfloat16_rn(sg * u);
+      const size_t o = (size_t)n * a.out_ld + (size_t)rb * 64 + r;
+      if (FUTR_DCHECK(o < a.out_cap, a.err)) a.out[o] = __float2bfloat16_rn(sg * u);
     }
   } else {
     if (rb == 0 && tid == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)

@@ -14,6 +14,7 @@ from typing import Optional, Sequence
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfutr.so")
+LIB_DEBUG_PATH = os.path.join(PKG, "libfutr_debug.so")
 
 FUTR_OK = 0
 FUTR_ERR_INVALID_ARG = 1
@@ -23,6 +24,8 @@ FUTR_ERR_OUT_OF_RANGE = 4
 FUTR_ERR_TIMEOUT = 5
 FUTR_ERR_BAD_BLOB = 6
 FUTR_ERR_NOT_PD = 7
+FUTR_ERR_CORRUPT = 8
+FUTR_ERR_BOUNDS = 9
 
 FUTR_PROJ_QKV, FUTR_PROJ_O, FUTR_PROJ_GATE, FUTR_PROJ_UP, FUTR_PROJ_DOWN = range(5)
 
@@ -86,12 +89,16 @@ _SIGS = {
 
 
 def lib() -> C.CDLL:
-    """Load libfutr.so (built by ``build.py``); raises if it is missing."""
+    """Load libfutr.so (built by ``build.py``), or its debug variant
+    libfutr_debug.so (``build.py --debug``: device bounds checks) when the
+    environment has FUTR_DEBUG=1; raises if that library is missing."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is not built; run int4_weight_kv_w4a16_gb300/build.py")
-        h = C.CDLL(LIB_PATH)
+        path = LIB_DEBUG_PATH if os.environ.get("FUTR_DEBUG") == "1" else LIB_PATH
+        if not os.path.exists(path):
+            flag = " --debug" if path == LIB_DEBUG_PATH else ""
+            raise RuntimeError(f"{path} is not built; run int4_weight_kv_w4a16_gb300/build.py{flag}")
+        h = C.CDLL(path)
         for name, (res, args) in _SIGS.items():
             fn = getattr(h, name)
             fn.restype = res

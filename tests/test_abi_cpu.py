@@ -44,6 +44,19 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(futr, n), n
 
 
+def test_debug_variant_builds_and_exports_the_same_symbols():
+    """libfutr_debug.so (-DFUTR_DEBUG: device bounds checks) builds from the
+    same sources and exports every declared entry point."""
+    path = build.build(debug=True)
+    assert os.path.basename(path) == "libfutr_debug.so"
+    D = C.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(D, n), n
+    D.futr_status_string.restype = C.c_char_p
+    assert b"bounds" in D.futr_status_string(futr.FUTR_ERR_BOUNDS)
+    assert b"guard" in D.futr_status_string(futr.FUTR_ERR_CORRUPT)
+
+
 def test_struct_sizes_match_binding(L):
     # futr_shape: 9 x 4 bytes; descriptors are plain data with 8-byte fields
     assert C.sizeof(futr.futr_shape) == 36
@@ -106,7 +119,8 @@ def test_kv_size_formula(L):
     n = futr.futr_kv_size(sh, 2, 3, 1000)  # capacity rounds up to 1008
     streams = 2 * 3 * 8 * 1008 * (128 + 4)
     rope = 1008 * 64 * 8
-    assert n >= streams + rope and n <= streams + rope + 1024
+    # + the error word and three 256-byte guards (one after each region), 256-byte aligned
+    assert n >= streams + rope + 16 + 3 * 256 and n <= streams + rope + 2048
 
 
 def test_kv_size_beyond_32_bits(L):
@@ -115,7 +129,7 @@ def test_kv_size_beyond_32_bits(L):
     n = futr.futr_kv_size(futr.make_shape(LLAMA70B), 80, 32, 65536)
     streams = 80 * 32 * 8 * 65536 * (128 + 4)
     assert streams > 2 ** 32
-    assert streams + 65536 * 64 * 8 <= n <= streams + 65536 * 64 * 8 + 1024
+    assert streams + 65536 * 64 * 8 <= n <= streams + 65536 * 64 * 8 + 2048
     # one position more than the supported capacity is refused
     sz = C.c_size_t(0)
     assert L.futr_kv_size(C.byref(futr.make_shape(LLAMA70B)), 80, 32, 65537, C.byref(sz)) == futr.FUTR_ERR_UNSUPPORTED
