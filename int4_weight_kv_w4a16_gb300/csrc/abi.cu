@@ -101,7 +101,8 @@ Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int
   const BlobSections sec = blob_sections(s);
   Plans p;
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
-  for (int i = 0; i < 4; ++i) p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
+  for (int i = 0; i < 4; ++i)
+    p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
   p.attn = plan_attention(s, batch, cap, n_sm, force_attn);
   p.blk = batch <= kBlockMaxBatch ? plan_block(s, batch, cap, n_sm, 0) : BlockPlan{};
   return p;
@@ -334,10 +335,10 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     A.part_cap = ws->part_bytes / 4;
     A.out_cap = (size_t)batch * out_ld[i];
 #ifdef FUTR_DEBUG
-    // FUTR_TEST_SHRINK_PART=1 (debug build, tests of the bounds checks only):
-    // the split records are checked against a region of one float, so the
-    // first record write fails its check and is skipped
-    if (env_int("FUTR_TEST_SHRINK_PART") == 1) A.part_cap = 1;
+    // FUTR_TEST_SHRINK_OUT=1 (debug build, tests of the bounds checks only):
+    // the outputs of O, gate/up and down are checked against a region of one
+    // element, so their first writes fail the check and are skipped
+    if (env_int("FUTR_TEST_SHRINK_OUT") == 1 && i > 0) A.out_cap = 1;
 #endif
     if (i == 0) {
       A.blob_magic = reinterpret_cast<const uint64_t*>(blob);

@@ -48,12 +48,123 @@ namespace futr {
 
 namespace {
 
+// ------------------------------------------------ cluster split-K tail --
+// The S CTAs of a row block form one thread-block cluster (cluster rank =
+// split index).  After its K-range each CTA leaves its partial tile [batch row]
+// [128 rows] and its sums of squares in its own shared memory; a cluster
+// barrier; then every CTA adds, for the outputs it owns, the S partials in
+// split order (distributed-shared-memory loads, all S in flight) and runs the
+// fused epilogue on them:
+//   RESID : rows [r*128/S, (r+1)*128/S) of the block, every batch row
+//   SWIGLU: outputs [r*64/S, (r+1)*64/S) (gate row j, up row 64 + j)
+//   QKV   : head tasks (batch row, head) r, r + S, ... (one warp each)
+// A second cluster barrier keeps every CTA's shared memory alive until the
+// others have read it.  Every thread of every CTA (the producer warp
+// included) reaches both barriers exactly once; a time-out anywhere in the
+// cluster is visible through the abort word after the first one, and then no
+// output is written.  No global partial records, counters or atomics.
+constexpr int kMaxProjCluster = 16;
+
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// Shared-memory address of `local` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cl_map(const void* local, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float cl_ld(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// sum over the cluster's S CTAs, in rank order from 0, of the float at `local`
+// (eight loads in flight per round)
+__device__ __forceinline__ float cl_sum(const float* local, int S) {
+  float acc = 0.f;
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s0 + s < S) v[s] = cl_ld(cl_map(local, s0 + s));
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s0 + s < S) acc += v[s];
+  }
+  return acc;
+}
+
+// The owned outputs of this CTA (rank `rank` of the cluster of row block rb),
+// from the S partial tiles `red` and sums of squares `ss`.  Consumer threads.
+template <int EPI>
+__device__ __forceinline__ void cluster_epilogue(const ProjArgs& a, const float* red, const float* ss, int rb,
+                                                 int S, int rank) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (EPI == kEpiResid) {
+    const int r0 = rank * kRowsPerBlock / S, nr = (rank + 1) * kRowsPerBlock / S - r0;
+    for (int e = tid; e < nr * a.batch; e += kCW * 32) {
+      const int n = e / nr, row = r0 + (e - n * nr);
+      const size_t o = (size_t)n * a.out_ld + (size_t)rb * kRowsPerBlock + row;
+      const float res = __bfloat162float(__ldcg(a.resid + o));
+      const float v = cl_sum(red + n * kRedLd + row, S);
+      if (FUTR_DCHECK(o < a.out_cap, a.err)) a.out[o] = __float2bfloat16_rn(res + v);
+    }
+  } else if (EPI == kEpiSwiglu) {
+    const int j0 = rank * 64 / S, nj = (rank + 1) * 64 / S - j0;
+    for (int e = tid; e < nj * a.batch; e += kCW * 32) {
+      const int n = e / nj, j = j0 + (e - n * nj);
+      const float g0 = cl_sum(red + n * kRedLd + j, S);
+      const float u0 = cl_sum(red + n * kRedLd + 64 + j, S);
+      const float sq = cl_sum(ss + n, S);
+      const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(sq, (float)a.K) + a.eps));
+      const float g = rn * g0;
+      const float u = rn * u0;
+      const float sg = __fdiv_rn(g, 1.0f + expf(-g));
+      const size_t o = (size_t)n * a.out_ld + (size_t)rb * 64 + j;
+      if (FUTR_DCHECK(o < a.out_cap, a.err)) a.out[o] = __float2bfloat16_rn(sg * u);
+    }
+  } else {
+    if (rb == 0 && rank == 0 && tid == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
+      set_err(a.err, FUTR_ERR_BAD_BLOB);
+    const int hpr = kRowsPerBlock / a.d, ntask = a.batch * hpr;
+    for (int task = rank + S * warp; task < ntask; task += S * kCW) {
+      const int n = task / hpr, hl = task - n * hpr, hg = rb * hpr + hl;
+      const HeadPre hp = head_pre(a, n, hg);
+      const float sq = cl_sum(ss + n, S);
+      const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(sq, (float)a.K) + a.eps));
+      if (a.d == 128) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = cl_sum(red + n * kRedLd + hl * 128 + lane + 32 * j, S) * rn;
+        qkv_head_core<4>(a, v, n, hg, hp);
+      } else {
+        float v[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) v[j] = cl_sum(red + n * kRedLd + hl * 64 + lane + 32 * j, S) * rn;
+        qkv_head_core<2>(a, v, n, hg, hp);
+      }
+    }
+  }
+}
+
 // NTP: batch tiles of 8 columns, 1..4; 0 = one batch row (one tile, the
 // activation row by a bulk copy)
+// Which instantiations reduce inside a cluster (see cluster_epilogue and the
+// planner); the others through global split records added by the last CTA of
+// the row block.
+template <int NTP, int EPI>
+constexpr bool cluster_reduce() {
+  return NTP != 0 && EPI != kEpiSwiglu;
+}
+
 template <int NTP, int EPI>
 __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* xmap) {
   constexpr int NT = NTP == 0 ? 1 : NTP;
   constexpr bool kRow1 = NTP == 0;
+  constexpr bool kCluster = cluster_reduce<NTP, EPI>();
   extern __shared__ __align__(16) uint8_t smem_raw[];
   // tensor copies want a 128-byte aligned destination: the base is rounded up
   // (one row takes only 16-byte aligned bulk copies and uses it as it is)
@@ -122,6 +233,13 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
     } else {
       pdl_wait();
     }
+    if (kCluster) {
+      // the cluster's two barriers (see cluster_epilogue)
+      cl_arrive();
+      cl_wait();
+      cl_arrive();
+      cl_wait();
+    }
     return;
   }
 
@@ -170,11 +288,30 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
     }
   }
   if (EPI != kEpiResid) ssq_to_smem<NT>(ssq, ss, a.batch);
-  // accumulator fragments -> epilogue tile [batch row][block row] (the ring,
+  if (!kCluster) {
+    // split records in global memory, the last CTA of the row block reduces
+    // (accumulator fragments -> epilogue tile in the ring, which every warp
+    // has left by then)
+    proj_tail<NT, EPI>(a, reinterpret_cast<float*>(smem), rb, a.S, sk, ss, flag, ok,
+                       [&](float* red) { acc_to_red<NT>(acc, red); }, []() {});
+    if (flag[1] && tid == 0) drain_after_timeout(smem, a.off_misc, a.ring);
+    return;
+  }
+  if (!ok) record_timeout(a.err);  // before the cluster barrier: the others see the abort word after it
+  // accumulator fragments -> partial tile [batch row][block row] (the ring,
   // which every warp has left by then)
-  proj_tail<NT, EPI>(a, reinterpret_cast<float*>(smem), rb, a.S, sk, ss, flag, ok,
-                     [&](float* red) { acc_to_red<NT>(acc, red); }, []() {});
-  if (flag[1] && tid == 0) drain_after_timeout(smem, a.off_misc, a.ring);
+  consumer_sync();
+  float* red = reinterpret_cast<float*>(smem);
+  acc_to_red<NT>(acc, red);
+  cl_arrive();  // this CTA's partial tile and sums of squares are complete
+  cl_wait();
+  const bool live = !aborted(a.err);
+  if (live) cluster_epilogue<EPI>(a, red, ss, rb, a.S, sk);
+  cl_arrive();  // done reading the other CTAs' shared memory
+  cl_wait();
+  // after a time-out (here or in another CTA, which stops this CTA's waits
+  // too), let this CTA's copies land before it exits
+  if (!live && tid == 0) drain_after_timeout(smem, a.off_misc, a.ring);
 }
 
 // ------------------------------------------------- tensor-core variant --
@@ -524,7 +661,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 }
 
 template <int NT, int EPI>
-__global__ void __launch_bounds__(kThreads) proj_kernel(const ProjArgs a, const __grid_constant__ CUtensorMap xmap) {
+__global__ void __launch_bounds__(kThreads, NT <= 1 ? 6 : 3) proj_kernel(const ProjArgs a, const __grid_constant__ CUtensorMap xmap) {
   proj_body<NT, EPI>(a, &xmap);
 }
 
@@ -554,6 +691,9 @@ cudaError_t configure(int dev) {
   e = cudaFuncSetAttribute(proj_entry<NT, EPI>(), cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
+  // clusters of up to 16 CTAs (the split-K clusters)
+  e = cudaFuncSetAttribute(proj_entry<NT, EPI>(), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
   configured.mark(dev);
   return cudaSuccess;
 }
@@ -565,16 +705,32 @@ cudaError_t launch_one(const ProjArgs& a, int grid, size_t smem, cudaStream_t st
   if (e != cudaSuccess) return e;
   e = configure<NT, EPI>(dev);
   if (e != cudaSuccess) return e;
+  // with the cluster reduction the S CTAs of a row block are one cluster
+  // (cluster_epilogue reads the shared memory of ranks 0..S-1, so the cluster
+  // size must be exactly S)
+  if (a.cluster != (cluster_reduce<NT, EPI>() ? 1 : 0)) return cudaErrorInvalidValue;  // fixed per instantiation
+  if (a.cluster && (a.S < 1 || a.S > kMaxProjCluster || grid % a.S != 0)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (a.cluster) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)a.S;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   CUtensorMap xmap;
   if (NT == 0)
     memset(&xmap, 0, sizeof(xmap));  // one row: no tensor copy
@@ -665,6 +821,72 @@ int resident_ctas(int nt, int epi, size_t smem) {
   });
 }
 
+// Largest split-K cluster the device schedules for this instantiation (at
+// most kMaxProjCluster).
+int max_proj_cluster(int nt, int epi, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  return remembered(occ_key(dev, 16 + nt, epi, smem), [&]() {
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMaxProjCluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+#define FUTR_CL(NT_, EPI_)                                                                   \
+  if (nt == NT_ && epi == EPI_) {                                                            \
+    e = configure<NT_, EPI_>(dev);                                                           \
+    if (e == cudaSuccess) e = cudaOccupancyMaxPotentialClusterSize(&n, proj_entry<NT_, EPI_>(), &cfg); \
+  }
+    FUTR_CL(0, 0) FUTR_CL(1, 0) FUTR_CL(2, 0) FUTR_CL(3, 0) FUTR_CL(4, 0)
+    FUTR_CL(0, 1) FUTR_CL(1, 1) FUTR_CL(2, 1) FUTR_CL(3, 1) FUTR_CL(4, 1)
+    FUTR_CL(0, 2) FUTR_CL(1, 2) FUTR_CL(2, 2) FUTR_CL(3, 2) FUTR_CL(4, 2)
+#undef FUTR_CL
+    if (e != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return 1;
+    }
+    return n < kMaxProjCluster ? n : kMaxProjCluster;
+  });
+}
+
+// Clusters of S CTAs of this instantiation that the device holds at once (a
+// cluster sits within one GPC, so this can be fewer than the resident CTAs
+// per SM x SMs / S).
+int active_clusters(int nt, int epi, size_t smem, int S) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return remembered(occ_key(dev, 64 + nt * 16 + S - 1, epi, smem), [&]() {
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(S * 64));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#define FUTR_AC(NT_, EPI_)                                                              \
+  if (nt == NT_ && epi == EPI_) {                                                       \
+    e = configure<NT_, EPI_>(dev);                                                      \
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, proj_entry<NT_, EPI_>(), &cfg); \
+  }
+    FUTR_AC(1, 0) FUTR_AC(2, 0) FUTR_AC(3, 0) FUTR_AC(4, 0)
+    FUTR_AC(1, 1) FUTR_AC(2, 1) FUTR_AC(3, 1) FUTR_AC(4, 1)
+    FUTR_AC(1, 2) FUTR_AC(2, 2) FUTR_AC(3, 2) FUTR_AC(4, 2)
+#undef FUTR_AC
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return n;
+  });
+}
+
 }  // namespace
 
 ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_split, int epi) {
@@ -707,13 +929,31 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   // next kernel start streaming its weights under programmatic launch).
   const int fit_max = std::max(1, std::min(16, 233472 / (int)(p.smem + 1024)));
   p.s_cap = std::min(p.n_groups, std::max(1, (4 * n_sm * fit_max + p.n_rb - 1) / p.n_rb));
+  // QKV, O and down on the mma.sync kernels from batch 2 on: the splits of a
+  // row block form one cluster and reduce in distributed shared memory, which
+  // removes the global records, the arrival and the reload from each tail and
+  // spreads the epilogue over the cluster (8B batch 8: 71.0 -> 61.7 µs per
+  // block-step, batch 32 ragged: 145 -> 124; the QKV epilogue of 32 sequences
+  // no longer runs in one CTA).  At batch 1 clusters of up to 16 CTAs are
+  // placed more slowly than single CTAs while the previous kernel still holds
+  // SM slots, which costs more than the shorter tail saves (8B: 52.8 vs 62.4
+  // µs), and gate/up (hundreds of row blocks, a short SwiGLU tail) lost 2-6 µs
+  // to whole-cluster waves: both keep the global records.
+  p.cluster = !p.tc && batch > 1 && epi != kEpiSwiglu;
   const int fit = p.tc ? resident_tc(epi, p.smem) : resident_ctas(batch == 1 ? 0 : p.nt, epi, p.smem);
+  const int s_max =
+      p.cluster ? std::min({p.s_cap, kMaxProjCluster, max_proj_cluster(batch == 1 ? 0 : p.nt, epi, p.smem)}) : p.s_cap;
   const long long slots = (long long)n_sm * std::min(fit > 0 ? fit : 1, fit_max);
   int best_s = 1;
   double best = 1e30;
-  for (int s = 1; s <= p.s_cap; ++s) {
+  for (int s = 1; s <= s_max; ++s) {
     const long long items = (long long)p.n_rb * s;
-    const long long waves = (items + slots - 1) / slots;
+    long long waves = (items + slots - 1) / slots;
+    if (p.cluster) {
+      // whole clusters per wave
+      const int c = active_clusters(p.nt, epi, p.smem, s);
+      if (c > 0) waves = std::max(waves, ((long long)p.n_rb + c - 1) / c);
+    }
     const int per = (p.n_groups + s - 1) / s;
     const double cost = (double)waves * (per + 3) * (s > 1 ? 1.1 : 1.0);
     if (cost < best - 1e-9) {
@@ -721,16 +961,19 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
       best_s = s;
     }
   }
-  if (force_split > 0) best_s = force_split < p.s_cap ? force_split : p.s_cap;
+  if (force_split > 0) best_s = force_split < s_max ? force_split : s_max;
   p.S = best_s;
   p.rec_floats = batch * kRecLd;
-  p.part_floats = (size_t)p.n_rb * p.S * p.rec_floats;
+  // split records in global memory (none with the cluster reduction); a
+  // workspace reserves them for s_cap whatever the mode
+  p.part_floats = p.cluster ? 0 : (size_t)p.n_rb * p.S * p.rec_floats;
   p.part_cap_floats = (size_t)p.n_rb * p.s_cap * p.rec_floats;
   return p;
 }
 
 cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream_t st, bool pdl) {
   a.S = p.S;
+  a.cluster = p.cluster ? 1 : 0;
   a.part_stride = p.S;
   a.n_groups = p.n_groups;
   a.ring = p.ring;

@@ -28,6 +28,7 @@ struct ProjArgs {
   unsigned* cnt;                 // arrival counters [n_rb]
   int* err;
   float eps;
+  int cluster;                   // the S CTAs of a row block form a cluster (reduction in shared memory)
   // extents the debug build checks accesses against: floats of `part`, rows
   // blocks of the section, elements of `out` (RESID / SWIGLU)
   size_t part_cap, out_cap;
@@ -53,6 +54,7 @@ struct ProjPlan {
   int n_rb, n_groups, nt, S, epi;
   int s_cap;                     // largest split any plan of this shape and batch can choose
   bool tc;                       // tensor-core kernel (batch 17..32)
+  bool cluster;                  // mma.sync kernel with the split-K reduction inside a cluster of S CTAs
   int ring, stage_bytes, off_misc, rec_floats;
   size_t smem;
   size_t part_floats;            // split records of this plan

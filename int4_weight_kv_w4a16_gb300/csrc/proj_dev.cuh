@@ -67,14 +67,13 @@ __device__ __forceinline__ void fill_head_cache(const ProjArgs& a, int rb, float
   }
 }
 
+// One head task of the QKV epilogue for one warp: v holds the head's d sums
+// times the RMSNorm factor (element lane + 32 j in v[j]); RoPE (q, k), the fp32
+// rotation, then q' to qrot or k, v as INT4 + fp16 scale into cache slot p.
 template <int J>
-__device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, int hl, int hg, float r,
-                                  const HeadPre& pre) {
+__device__ void qkv_head_core(const ProjArgs& a, float (&v)[J], int n, int hg, const HeadPre& pre) {
   constexpr int d = 32 * J;
   const int lane = threadIdx.x & 31;
-  float v[J];
-#pragma unroll
-  for (int j = 0; j < J; ++j) v[j] = red[n * kRedLd + hl * d + lane + 32 * j] * r;
   const int p = pre.p;
   const bool is_q = hg < a.Hq, is_k = !is_q && hg < a.Hq + a.Hkv;
   const bool p_ok = p >= 0 && p < a.kv.cap;
@@ -108,6 +107,33 @@ __device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, in
     store_k_token<J>(a.kv.stream(n, hg - a.Hq), a.kv.cap, p, code, s, scratch[warp]);
   else
     store_v_token<J>(a.kv.stream(n, hg - a.Hq - a.Hkv), a.kv.cap, p, code, s, scratch[warp]);
+}
+
+// The same from the epilogue tile of the last CTA (global split-K tail).
+template <int J>
+__device__ void qkv_head_epilogue(const ProjArgs& a, const float* red, int n, int hl, int hg, float r,
+                                  const HeadPre& pre) {
+  constexpr int d = 32 * J;
+  const int lane = threadIdx.x & 31;
+  float v[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) v[j] = red[n * kRedLd + hl * d + lane + 32 * j] * r;
+  qkv_head_core<J>(a, v, n, hg, pre);
+}
+
+// Position and RoPE factors of head hg for batch row n, as fill_head_cache
+// stores them (q and k heads rotate by position; v heads get (1, 0)).
+__device__ __forceinline__ HeadPre head_pre(const ProjArgs& a, int n, int hg) {
+  const int lane = threadIdx.x & 31, half = a.d / 2;
+  HeadPre hp;
+  hp.p = a.pos[n];
+  hp.cs[0] = hp.cs[1] = make_float2(1.f, 0.f);
+  if (hg < a.Hq + a.Hkv) {
+    const int pp = hp.p >= 0 && hp.p < a.kv.cap ? hp.p : 0;
+    hp.cs[0] = a.rope[(size_t)pp * half + lane];
+    if (half > 32) hp.cs[1] = a.rope[(size_t)pp * half + lane + 32];
+  }
+  return hp;
 }
 
 // The producer lane's count of issued ring stages, for the drain after a

@@ -27,10 +27,10 @@ def run(name, shrink=False):
     pd = torch.from_numpy(pos).cuda()
     y = torch.empty_like(xd)
     if shrink:
-        os.environ["FUTR_TEST_SHRINK_PART"] = "1"
+        os.environ["FUTR_TEST_SHRINK_OUT"] = "1"
     futr.futr_decode_block(xd, gpu.blob, gpu.kv, 0, b, pd, y, gpu.ws)
     st = futr.futr_check(gpu.ws, gpu.kv)
-    os.environ.pop("FUTR_TEST_SHRINK_PART", None)
+    os.environ.pop("FUTR_TEST_SHRINK_OUT", None)
     # a second step after the check (counters and error words start over)
     futr.futr_decode_block(xd, gpu.blob, gpu.kv, 0, b, pd, y, gpu.ws)
     st2 = futr.futr_check(gpu.ws, gpu.kv)

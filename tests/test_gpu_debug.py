@@ -56,9 +56,10 @@ def test_debug_build_matches_release_bit_for_bit(tmp_path):
 
 
 def test_debug_build_bounds_check_reports_and_recovers(tmp_path):
-    """FUTR_TEST_SHRINK_PART=1 (debug build only) checks the split records
-    against a one-float region: the first record write fails its check, is
-    skipped, and the step reports FUTR_ERR_BOUNDS; the next step is clean."""
+    """FUTR_TEST_SHRINK_OUT=1 (debug build only) checks the outputs of O,
+    gate/up and down against a one-element region: their first writes fail
+    the check and are skipped, the step reports FUTR_ERR_BOUNDS, and the next
+    step is clean."""
     dbg = _child(tmp_path, "shrink", FUTR_DEBUG="1", FUTR_CHILD_SHRINK="1")
     ok = _child(tmp_path, "plain", FUTR_DEBUG="1")
     for name in ("toy_b3", "8b_b1"):
