@@ -205,6 +205,19 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
 
   if (sp == 0) {
     // ---- the leader merges the NC ranges in range order
+    float4* mO4 = reinterpret_cast<float4*>(mO);
+    // With at most one float4 of O per thread (up to 4 heads of 128 dims),
+    // its NC range values are loaded together with the ranges' (m, l), before
+    // the weights are known: one round of remote loads instead of two.
+    const int n4 = Gv * D / 4;
+    const bool one = n4 <= kAttnThreads;
+    float4 v[kMaxCluster];
+    if (one && tid < n4) {
+      v[0] = mO4[tid];
+#pragma unroll
+      for (int r = 1; r < kMaxCluster; ++r)
+        if (r < NC) v[r] = ld_dsmem4(&mO4[tid], (uint32_t)r);
+    }
     for (int i = tid; i < NC * G; i += kAttnThreads) {
       const int r = i / G, h = i - r * G;
       if (h >= Gv) continue;
@@ -226,24 +239,37 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
       cm[tid] = Lr;  // total normalizer of head row tid
     }
     __syncthreads();
-    float4* mO4 = reinterpret_cast<float4*>(mO);
-    for (int e4 = tid; e4 < Gv * D / 4; e4 += kAttnThreads) {
-      const int h = (4 * e4) / D;
-      // every range's value first (independent remote loads in flight), then
-      // the weighted sum in range order
-      float4 v[kMaxCluster];
-      v[0] = mO4[e4];
+    if (one) {
+      if (tid < n4) {
+        const int h = (4 * tid) / D;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int r = 1; r < kMaxCluster; ++r)
-        if (r < NC) v[r] = ld_dsmem4(&mO4[e4], (uint32_t)r);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < NC) {
+            const float wt = wm[r * G + h];
+            acc.x += v[r].x * wt; acc.y += v[r].y * wt; acc.z += v[r].z * wt; acc.w += v[r].w * wt;
+          }
+        mO4[tid] = acc;  // only this thread reads or writes this float4
+      }
+    } else {
+      for (int e4 = tid; e4 < n4; e4 += kAttnThreads) {
+        const int h = (4 * e4) / D;
+        // every range's value first (independent remote loads in flight), then
+        // the weighted sum in range order
+        float4 w[kMaxCluster];
+        w[0] = mO4[e4];
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < NC) {
-          const float wt = wm[r * G + h];
-          acc.x += v[r].x * wt; acc.y += v[r].y * wt; acc.z += v[r].z * wt; acc.w += v[r].w * wt;
-        }
-      mO4[e4] = acc;
+        for (int r = 1; r < kMaxCluster; ++r)
+          if (r < NC) w[r] = ld_dsmem4(&mO4[e4], (uint32_t)r);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < NC) {
+            const float wt = wm[r * G + h];
+            acc.x += w[r].x * wt; acc.y += w[r].y * wt; acc.z += w[r].z * wt; acc.w += w[r].w * wt;
+          }
+        mO4[e4] = acc;
+      }
     }
     __syncthreads();
     // ---- normalize, rotate back, store bf16 (an empty context stores zeros)

@@ -415,11 +415,27 @@ def test_decode_host_entry_matches_device_entry():
     pos = np.array([5, 6, 7], np.int32)
     yd = gpu.decode(x, pos).cpu().numpy().view(np.uint16)
     # run again through the host-buffer entry (same cache slot is rewritten identically)
+    # pinned buffers, repeated calls
     xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
     ph = torch.from_numpy(pos.copy()).pin_memory()
     yh = torch.empty_like(xh).pin_memory()
+    for _ in range(4):
+        yh.zero_()
+        futr.futr_decode_block_host(xh, gpu.blob, gpu.kv, 0, batch, ph, yh, gpu.ws)
+        np.testing.assert_array_equal(yh.numpy().view(np.uint16), yd)
+    # new host contents, same buffers
+    x2 = inputs.activations(shape, batch, 5)
+    y2 = gpu.decode(x2, pos).cpu().numpy().view(np.uint16)
+    xh.copy_(torch.from_numpy(x2.view(np.int16).copy()))
     futr.futr_decode_block_host(xh, gpu.blob, gpu.kv, 0, batch, ph, yh, gpu.ws)
-    np.testing.assert_array_equal(yh.numpy().view(np.uint16), yd)
+    np.testing.assert_array_equal(yh.numpy().view(np.uint16), y2)
+    # pageable buffers
+    xp, pp, yp = xh.clone(), ph.clone(), torch.empty_like(xh)
+    assert not xp.is_pinned()
+    for _ in range(2):
+        futr.futr_decode_block_host(xp, gpu.blob, gpu.kv, 0, batch, pp, yp, gpu.ws)
+        np.testing.assert_array_equal(yp.numpy().view(np.uint16), y2)
+    assert futr.futr_check(gpu.ws, gpu.kv) == 0
 
 
 def test_workspace_size_ignores_forced_splits(monkeypatch):
