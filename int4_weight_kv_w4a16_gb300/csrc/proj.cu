@@ -951,7 +951,7 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
     long long waves = (items + slots - 1) / slots;
     if (p.cluster) {
       // whole clusters per wave
-      const int c = active_clusters(p.nt, epi, p.smem, s);
+      const int c = active_clusters(batch == 1 ? 0 : p.nt, epi, p.smem, s);
       if (c > 0) waves = std::max(waves, ((long long)p.n_rb + c - 1) / c);
     }
     const int per = (p.n_groups + s - 1) / s;
