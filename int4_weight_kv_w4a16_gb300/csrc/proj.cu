@@ -247,6 +247,14 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
   pdl_wait();
   const unsigned long long deadline = global_ns() + kWaitNs;
   bool ok = true;
+  // QKV with global records (batch 1): warp w's head task's position and RoPE
+  // factors, loaded now and used by the epilogue (their latency hides under
+  // the K-loop instead of lengthening the tail)
+  HeadPre hp_pre{};
+  if (EPI == kEpiQkv && !kCluster) {
+    const int hpr = kRowsPerBlock / a.d;
+    if (warp < a.batch * hpr) hp_pre = head_pre(a, warp / hpr, rb * hpr + warp % hpr);
+  }
 
   float acc[kMT][NT][4];
 #pragma unroll
@@ -293,7 +301,8 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
     // (accumulator fragments -> epilogue tile in the ring, which every warp
     // has left by then)
     proj_tail<NT, EPI>(a, reinterpret_cast<float*>(smem), rb, a.S, sk, ss, flag, ok,
-                       [&](float* red) { acc_to_red<NT>(acc, red); }, []() {});
+                       [&](float* red) { acc_to_red<NT>(acc, red); }, []() {},
+                       EPI == kEpiQkv ? &hp_pre : nullptr);
     if (flag[1] && tid == 0) drain_after_timeout(smem, a.off_misc, a.ring);
     return;
   }

@@ -194,9 +194,13 @@ __device__ __forceinline__ void issue_tile(const ProjArgs& a, const CUtensorMap*
 // consumer thread of the CTA that ran the epilogue, once its writes are issued.
 // After a time-out (flag[1] set) it returns at once, writing nothing: the
 // caller then lets its in-flight copies land (drain_after_timeout).
+// pre (QKV, at most one head task per consumer warp): this warp's task's
+// position and RoPE factors, loaded by the caller ahead of time; otherwise
+// they are loaded during the arrival.
 template <int NT, int EPI, class WriteRed, class Done>
 __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb, int S, int slot, float* ss,
-                                          int* flag, bool ok, WriteRed&& write_red, Done&& done) {
+                                          int* flag, bool ok, WriteRed&& write_red, Done&& done,
+                                          const HeadPre* pre = nullptr) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the residual rows of this block (RESID): with one batch tile loaded now,
   // overlapping the split handshake; with more, in one burst after the
@@ -217,6 +221,7 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
   // the epilogue tile and the split-sum groups (the ring is free by then)
   float2* hcs = reinterpret_cast<float2*>(red + NT * 8 * kRedLd + 4 * kCW * 32);
   int* hpos = reinterpret_cast<int*>(hcs + a.batch * (kRowsPerBlock / a.d) * 64);
+  const bool have_pre = EPI == kEpiQkv && pre != nullptr && a.batch * (kRowsPerBlock / a.d) <= kCW;
   if (!ok) {
     record_timeout(a.err);
     flag[1] = 1;
@@ -249,7 +254,7 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
     consumer_sync();
     if (tid == 0)
       flag[0] = atom_add_acq_rel_gpu(&a.cnt[rb], 1u) == (unsigned)(S - 1) ? 1 : 0;
-    else if (EPI == kEpiQkv)
+    else if (EPI == kEpiQkv && !have_pre)
       fill_head_cache(a, rb, hcs, hpos, tid - 1, kCW * 32 - 1);  // overlaps the arrival
     consumer_sync();
     if (!flag[0]) return;
@@ -342,7 +347,7 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
   }
 
   if (!kEarly) load_resid();
-  if (EPI == kEpiQkv && S == 1) {
+  if (EPI == kEpiQkv && S == 1 && !have_pre) {
     fill_head_cache(a, rb, hcs, hpos, tid, kCW * 32);
     consumer_sync();
   }
@@ -374,9 +379,13 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
       const int hg = rb * hpr + hl;
       const float rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(ss[n], (float)a.K) + a.eps));
       HeadPre hp;
-      hp.p = hpos[task];
-      hp.cs[0] = hcs[(task * 2) * 32 + lane];
-      hp.cs[1] = hcs[(task * 2 + 1) * 32 + lane];
+      if (have_pre) {
+        hp = *pre;  // task == warp
+      } else {
+        hp.p = hpos[task];
+        hp.cs[0] = hcs[(task * 2) * 32 + lane];
+        hp.cs[1] = hcs[(task * 2 + 1) * 32 + lane];
+      }
       if (a.d == 128)
         qkv_head_epilogue<4>(a, red, n, hl, hg, rn, hp);
       else
