@@ -150,8 +150,6 @@ __device__ __forceinline__ void cluster_epilogue(const ProjArgs& a, const float*
   }
 }
 
-// NTP: batch tiles of 8 columns, 1..4; 0 = one batch row (one tile, the
-// activation row by a bulk copy)
 // Which instantiations reduce inside a cluster (see cluster_epilogue and the
 // planner); the others through global split records added by the last CTA of
 // the row block.
@@ -159,6 +157,9 @@ template <int NTP, int EPI>
 constexpr bool cluster_reduce() {
   return NTP != 0 && EPI != kEpiSwiglu;
 }
+
+// NTP: batch tiles of 8 columns, 1..4; 0 = one batch row (one tile, the
+// activation row by a bulk copy)
 
 template <int NTP, int EPI>
 __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* xmap) {
