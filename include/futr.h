@@ -273,9 +273,12 @@ futr_status futr_decode_block_timed(const uint16_t* x, const void* blob, const f
                                     float* stage_ms_host);
 
 /* As futr_decode_block with HOST input and output: copies x_host (bf16
- * [batch][H]) and pos_host (int32 [batch]) into the workspace, runs the block,
- * copies y back to y_host and synchronizes `stream`.  Pinned host buffers give
- * asynchronous copies. */
+ * [batch][H]) into the workspace, runs the block on pos_host (int32 [batch])
+ * and writes y_host, and synchronizes `stream`.  When pos_host and y_host are
+ * both page-locked and mapped for the device (cudaHostAlloc / cudaHostRegister
+ * memory on a unified-address system), the kernels read pos and write y there
+ * directly; otherwise they are copied through the workspace's staging rows.
+ * y_host must not be read before the call returns. */
 futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, const futr_kv* kv,
                                    int32_t layer, int32_t batch, const int32_t* pos_host,
                                    uint16_t* y_host, const futr_ws* ws, void* stream);

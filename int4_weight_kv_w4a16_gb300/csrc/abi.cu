@@ -435,6 +435,17 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
   return FUTR_OK;
 }
 
+// The device address of page-locked host memory that the device can access
+// (mapped), or nullptr for any other pointer.
+void* mapped_ptr(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 }  // namespace
 
 extern "C" {
@@ -669,11 +680,17 @@ futr_status futr_decode_block_host(const uint16_t* x_host, const void* blob, con
   uint16_t* yd = at<uint16_t>(ws->base, ws->off_yout);
   int32_t* pd = at<int32_t>(ws->base, ws->off_pos);
   if (cudaMemcpyAsync(xd, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return FUTR_ERR_CUDA;
-  if (cudaMemcpyAsync(pd, pos_host, (size_t)batch * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  // pinned (page-locked, device-mapped) pos and y: the kernels read pos and
+  // write y in host memory directly (plain loads and stores), which saves two
+  // copies per call; otherwise both go through the workspace's staging rows
+  const int32_t* pos_dev = static_cast<const int32_t*>(mapped_ptr(pos_host));
+  uint16_t* y_dev = static_cast<uint16_t*>(mapped_ptr(y_host));
+  const bool direct = pos_dev && y_dev;
+  if (!direct && cudaMemcpyAsync(pd, pos_host, (size_t)batch * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FUTR_ERR_CUDA;
-  st = run_block(xd, blob, kv, layer, batch, pd, yd, ws, s, nullptr);
+  st = run_block(xd, blob, kv, layer, batch, direct ? pos_dev : pd, direct ? y_dev : yd, ws, s, nullptr);
   if (st != FUTR_OK) return st;
-  if (cudaMemcpyAsync(y_host, yd, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return FUTR_ERR_CUDA;
+  if (!direct && cudaMemcpyAsync(y_host, yd, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return FUTR_ERR_CUDA;
   return cuda_status(cudaStreamSynchronize(s));
 }
 
