@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
   __syncthreads();
 
   // ---- merge the 4 warps: (mO, mm, ml) of this range
-  merge_warps(cm, cl, co, mO, mm, ml, G, Gv, D, tid, kAttnThreads);
+  merge_warps(cm, cl, co, mO, mm, ml, wm, G, Gv, D, tid, kAttnThreads, []() { __syncthreads(); });
   __syncthreads();
   if (NC > 1) cluster_sync_all();  // every range's (mO, mm, ml) is complete
 

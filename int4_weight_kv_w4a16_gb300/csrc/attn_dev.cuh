@@ -253,25 +253,33 @@ struct AttnWarp {
 };
 
 // The consumer warps' (m, l, O) rows merged into (mO [Gv][D], mm, ml [Gv]):
-// items first, first + stride, ...
+// threads first, first + stride, ... of the caller's group.  The weights of
+// each (warp, head), exp2(m_w - M), are computed once per head into
+// wbuf [kAttnCW][G] (between two `sync` calls of the whole group), then every
+// element adds the warps' rows in warp order.
+template <class Sync>
 __device__ __forceinline__ void merge_warps(const float* cm, const float* cl, const float* co, float* mO, float* mm,
-                                            float* ml, int G, int Gv, int D, int first, int stride) {
-  for (int e = first; e < Gv * D; e += stride) {
-    const int r = e / D, i = e % D;
+                                            float* ml, float* wbuf, int G, int Gv, int D, int first, int stride,
+                                            Sync&& sync) {
+  for (int r = first; r < Gv; r += stride) {
     float M = -INFINITY;
     for (int w = 0; w < kAttnCW; ++w) M = fmaxf(M, cm[w * G + r]);
-    float Lr = 0.f, Or = 0.f;
+    float Lr = 0.f;
     for (int w = 0; w < kAttnCW; ++w) {
       const float mw = cm[w * G + r];
       const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      wbuf[w * G + r] = wt;
       Lr += cl[w * G + r] * wt;
-      Or += co[(w * G + r) * D + i] * wt;
     }
+    mm[r] = M;
+    ml[r] = Lr;
+  }
+  sync();
+  for (int e = first; e < Gv * D; e += stride) {
+    const int r = e / D, i = e % D;
+    float Or = 0.f;
+    for (int w = 0; w < kAttnCW; ++w) Or += co[(w * G + r) * D + i] * wbuf[w * G + r];
     mO[e] = Or;
-    if (i == 0) {
-      mm[r] = M;
-      ml[r] = Lr;
-    }
   }
 }
 

@@ -372,7 +372,7 @@ __device__ __forceinline__ void attn_work(const BlockArgs& a, const AttnItem& it
   }
   aw.finish(cm, cl, co, G, Gv);
   consumer_sync();
-  merge_warps(cm, cl, co, mO, mm, ml, G, Gv, D, tid, kBlkCW * 32);
+  merge_warps(cm, cl, co, mO, mm, ml, wgt, G, Gv, D, tid, kBlkCW * 32, []() { consumer_sync(); });
   consumer_sync();
   // this range's record: m [G], l [G], O [G][D]
   float* rec = a.apart + ((size_t)ctx * a.NC + it.r) * a.arec_floats;
