@@ -67,6 +67,18 @@ constexpr int kMaxProjCluster = 16;
 
 __device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// The second barrier publishes nothing: every value this CTA read from the
+// others' shared memory has been consumed by the stores before it (so those
+// loads have completed), so its arrival needs no release.  (The debug build,
+// whose failed checks skip stores and leave loaded values unused, keeps the
+// release.)
+__device__ __forceinline__ void cl_arrive_relaxed() {
+#ifdef FUTR_DEBUG
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+#else
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+#endif
+}
 
 // Shared-memory address of `local` in the CTA of cluster rank `rank`.
 __device__ __forceinline__ uint32_t cl_map(const void* local, int rank) {
@@ -238,7 +250,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
       // the cluster's two barriers (see cluster_epilogue)
       cl_arrive();
       cl_wait();
-      cl_arrive();
+      cl_arrive_relaxed();
       cl_wait();
     }
     return;
@@ -317,7 +329,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
   cl_wait();
   const bool live = !aborted(a.err);
   if (live) cluster_epilogue<EPI>(a, red, ss, rb, a.S, sk);
-  cl_arrive();  // done reading the other CTAs' shared memory
+  cl_arrive_relaxed();  // done reading the other CTAs' shared memory
   cl_wait();
   // after a time-out (here or in another CTA, which stops this CTA's waits
   // too), let this CTA's copies land before it exits
