@@ -46,6 +46,13 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The closing barrier publishes nothing: every value the leader read from the
+// other CTAs' shared memory has been consumed by its stores before it, so the
+// arrival needs no release.
+__device__ __forceinline__ void cluster_sync_exit() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
@@ -285,7 +292,7 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
     }
     if (!pos_ok && kvh == 0 && tid == 0) set_err(a.err, FUTR_ERR_OUT_OF_RANGE);
   }
-  if (NC > 1) cluster_sync_all();  // the leader is done reading the other CTAs' shared memory
+  if (NC > 1) cluster_sync_exit();  // the leader is done reading the other CTAs' shared memory
   if (s_timeout && tid == 0) drain_ring(full, kAttnRing, s_issued);
 }
 
