@@ -95,9 +95,12 @@ struct Plans {
   ProjPlan proj[4];  // QKV, O, GU, DOWN
   AttnPlan attn;
   BlockPlan blk;     // the persistent whole-block kernel (batch <= 16)
+  // the five-kernel path at batch 1: QKV writes its split records only and
+  // the attention kernel adds them and runs the head epilogue
+  bool qkv_defer;
 };
 
-Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int force_attn) {
+Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int force_attn, bool allow_defer) {
   const BlobSections sec = blob_sections(s);
   Plans p;
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
@@ -105,25 +108,32 @@ Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int
     p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
   p.attn = plan_attention(s, batch, cap, n_sm, force_attn);
   p.blk = batch <= kBlockMaxBatch ? plan_block(s, batch, cap, n_sm, 0) : BlockPlan{};
+  // one cluster per kv-head (so one CTA forms each new token) and records
+  // that exist (split QKV, global reduction)
+  const ProjPlan& q = p.proj[0];
+  p.qkv_defer = allow_defer && batch == 1 && p.attn.one_sub && !q.tc && !q.cluster && q.S > 1;
   return p;
 }
 
 // Launch plans of one decode call.  FUTR_SPLITK / FUTR_ATTN_SPLIT force the
-// split-K and context-range counts (within the planner's bounds); plans are
-// kept per (shape, batch, capacity, SM count, forced counts), so a repeated
-// call only looks its plan up.
+// split-K and context-range counts (within the planner's bounds);
+// FUTR_QKV_DEFER=0 keeps the QKV head epilogue in the QKV kernel at batch 1.
+// Plans are kept per (shape, batch, capacity, SM count, these settings), so a
+// repeated call only looks its plan up.
 Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
   const int force = env_int("FUTR_SPLITK"), force_attn = env_int("FUTR_ATTN_SPLIT");
-  using Key = std::tuple<std::string, int, int, int, int, int>;
+  const int defer = env_int_or("FUTR_QKV_DEFER", 1) != 0 ? 1 : 0;
+  using Key = std::tuple<std::string, int, int, int, int, int, int>;
   static std::mutex mu;
   static std::map<Key, Plans> cache;
-  const Key key(std::string(reinterpret_cast<const char*>(&s), sizeof(s)), batch, cap, n_sm, force, force_attn);
+  const Key key(std::string(reinterpret_cast<const char*>(&s), sizeof(s)), batch, cap, n_sm, force, force_attn,
+                defer);
   {
     std::lock_guard<std::mutex> g(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  const Plans p = plan_all(s, batch, cap, n_sm, force, force_attn);
+  const Plans p = plan_all(s, batch, cap, n_sm, force, force_attn, defer != 0);
   std::lock_guard<std::mutex> g(mu);
   if (cache.size() > 4096) cache.clear();
   return cache.emplace(key, p).first->second;
@@ -164,7 +174,7 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
   const BlobSections sec = blob_sections(s);
   uint64_t n_ctx_max = 0;
   for (int b = 1; b <= max_batch; ++b) {
-    const Plans p = plan_all(s, b, cap, n_sm, 0, 0);
+    const Plans p = plan_all(s, b, cap, n_sm, 0, 0, true);
     for (int i = 0; i < 4; ++i)
       if (p.proj[i].s_cap > 1 && p.proj[i].part_cap_floats > part) part = p.proj[i].part_cap_floats;
     if (p.attn.part_floats > apart) apart = p.attn.part_floats;
@@ -413,6 +423,19 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
   for (int i = 0; i < 4; ++i)
     if (P.proj[i].S > 1 && P.proj[i].part_floats * 4 > ws->part_bytes) return FUTR_ERR_INVALID_ARG;
   if (P.attn.part_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
+  if (P.qkv_defer) {
+    // QKV leaves its records (in `part`, which O overwrites only after the
+    // attention kernel has completed) to the attention kernel
+    PA[0].defer = 1;
+    AT.qkv_part = part;
+    AT.qkv_S = P.proj[0].S;
+    AT.qkv_stride = P.proj[0].S;
+    AT.qkv_rec_floats = P.proj[0].rec_floats;
+    AT.qkv_part_cap = ws->part_bytes / 4;
+    AT.hidden = s.hidden;
+    AT.eps = s.rms_eps;
+    AT.rope = PA[0].rope;
+  }
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
   static const char* const names[4] = {"futr.qkv", "futr.o", "futr.gate_up", "futr.down"};
   cudaError_t e;

@@ -34,6 +34,14 @@
 // stores bf16; a second cluster barrier keeps every CTA's shared memory alive
 // until the leader is done.  No CTA leaves early, so every thread reaches
 // both barriers; the ring waits are bounded.
+//
+// At batch 1 the QKV projection leaves its split-K records (AttnArgs::qkv_part)
+// and the head epilogue runs here, after the wait: every CTA adds the records
+// of its query heads, applies the RMSNorm factor, RoPE and the rotation and
+// builds the query fragments from shared memory; in the CTA of the last range
+// the producer warp forms the new token's INT4 key and value, and the consumer
+// warp whose sub-tile holds that position patches them into its ring stage
+// (the copy of that slot predates them) and writes them into the cache.
 #include "futr_internal.cuh"
 #include "proj.cuh"
 #include "attn_dev.cuh"
@@ -74,6 +82,97 @@ __device__ __forceinline__ float4 ld_dsmem4(const float4* local, uint32_t rank) 
   return v;
 }
 
+// ------------------------------------ QKV head epilogue (batch 1, deferred) --
+// The QKV projection left its split records (ProjArgs::defer).  Head task i of
+// this CTA: query head hq0 + i for i < Gv, then (kv) the key and the value
+// head of kv-head kvh.  qs[i * D + r] = the sum over the splits (in split
+// order) of row r of task i's head, batch row b; *ss = the sum of squares of
+// x.  All threads of the CTA; loads of 8 splits in flight per item.
+template <int D>
+__device__ __forceinline__ void sum_qkv_records(const AttnArgs& a, int b, int hq0, int Gv, int kvh, bool kv,
+                                                float* qs, float* ss) {
+  constexpr int C = D / 4;  // float4 columns of a head
+  const int hpr = kRowsPerBlock / D, nt = Gv + (kv ? 2 : 0), S = a.qkv_S;
+  const size_t step = (size_t)a.qkv_rec_floats / 4;
+  for (int e = threadIdx.x; e < nt * C + 1; e += kAttnThreads) {
+    int rb = hq0 / hpr, col = kRecCols - 1;  // the last item: (sum of squares, 0, 0, 0)
+    if (e < nt * C) {
+      const int i = e / C, c = e - i * C;
+      const int hg = i < Gv ? hq0 + i : (i == Gv ? a.Hq + kvh : a.Hq + a.Hkv + kvh);
+      rb = hg / hpr;
+      col = (hg - rb * hpr) * C + c;
+    }
+    // debug build: the records read lie inside the region
+    if (!FUTR_DCHECK(((size_t)rb * a.qkv_stride + S) * a.qkv_rec_floats <= a.qkv_part_cap &&
+                         (size_t)(b + 1) * kRecLd <= (size_t)a.qkv_rec_floats,
+                     a.err))
+      continue;
+    const float4* src = reinterpret_cast<const float4*>(a.qkv_part + (size_t)rb * a.qkv_stride * a.qkv_rec_floats +
+                                                        (size_t)b * kRecLd) + col;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < S) v[j] = __ldcg(src + (size_t)(s0 + j) * step);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < S) {
+          acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+        }
+    }
+    if (e < nt * C)
+      reinterpret_cast<float4*>(qs)[e] = acc;
+    else
+      *ss = acc.x;
+  }
+}
+
+// One head task (one warp): v[j] = element lane + 32 j of the head's sums
+// times the RMSNorm factor rn, RoPE (rotate-half, dims i and i + D/2: element
+// j pairs j + J/2; cs[j] holds (cos, sin) of dims lane + 32 j) for query and
+// key heads, then the fp32 rotation.
+template <int D>
+__device__ __forceinline__ void head_from_sums(float (&v)[D / 32], const float* sums, float rn, bool rope,
+                                               const float2 (&cs)[2], const AttnArgs& a) {
+  constexpr int J = D / 32;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < J; ++j) v[j] = sums[lane + 32 * j] * rn;
+  if (rope) {
+#pragma unroll
+    for (int j = 0; j < J / 2; ++j) {
+      const float x1 = v[j], x2 = v[j + J / 2];
+      v[j] = x1 * cs[j].x - x2 * cs[j].y;
+      v[j + J / 2] = x2 * cs[j].x + x1 * cs[j].y;
+    }
+  }
+  warp_fwht<J>(v, a.nh, a.had_c);
+}
+
+// The new token (position p, offset r = p - c0 in the tile at c0) into a ring
+// stage that holds its tile (one warp): key codes, value nibbles and both
+// scales, from tok[0] / tok[1] (int8 codes, dim order) and toks.
+template <int D>
+__device__ __forceinline__ void patch_new_token(uint8_t* st, int r, int p, const int8_t (*tok)[D],
+                                                const __half* toks) {
+  using Lay = AttnLayout<D>;
+  const int lane = threadIdx.x & 31;
+  uint32_t* kw = reinterpret_cast<uint32_t*>(st + (size_t)r * (D / 2));
+  if (lane < D / 8) kw[lane] = k_token_word<D>(tok[0], lane);
+  uint32_t* vt = reinterpret_cast<uint32_t*>(st + Lay::kCodes + (size_t)(r >> 4) * (8 * D));
+  for (int w = lane; w < 8 * (D / 16); w += 32) {
+    const VWord vw = v_token_word<D>(tok[1], p, w);
+    vt[vw.off] = (vt[vw.off] & ~vw.mask) | vw.bits;
+  }
+  if (lane == 0) {
+    __half* ksc = reinterpret_cast<__half*>(st + 2 * Lay::kCodes);
+    ksc[r] = toks[0];
+    ksc[kTilePos + r] = toks[1];
+  }
+  __syncwarp();
+}
+
 // NTQ: n-tiles of query columns (1: at most 4 heads, 2: at most 8).
 template <int D, int NTQ>
 __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(const AttnArgs a) {
@@ -104,11 +203,19 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
   // ring stages the producer issued, and whether some wait of this CTA ran out
   // (then the CTA lets the issued copies land before it exits)
   __shared__ int s_issued, s_timeout;
+  // deferred QKV epilogue: the head tasks' sums (then q'), the sum of squares
+  // of x, the new token's codes and scales and their arrival
+  __shared__ __align__(16) float s_qs[(4 * NTQ + 2) * D];
+  __shared__ float s_ss;
+  __shared__ int8_t s_tok[2][D];
+  __shared__ __half s_toks[2];
+  __shared__ __align__(8) uint64_t s_kvready;
   if (tid == 0) {
     for (int i = 0; i < kAttnRing; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kAttnCW);
     }
+    mbar_init(&s_kvready, 1);
     fence_mbar_init();
     s_issued = 0;
     s_timeout = 0;
@@ -124,7 +231,7 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
   const int L = pos_ok ? p + 1 : 0;
   const int T = (L + kTilePos - 1) / kTilePos;
   const int tile0 = (int)((long long)sp * T / NC), ntiles = (int)((long long)(sp + 1) * T / NC) - tile0;
-  const uint8_t* strm = a.kv.stream(b, kvh);
+  uint8_t* strm = a.kv.stream(b, kvh);
   if (warp == kAttnCW && lane == 0) {
     for (int i = 0; i < ntiles && i < kAttnRing; ++i) {
       const int c0 = (tile0 + i) * kTilePos;
@@ -136,28 +243,64 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
       l2_prefetch(strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb);
     }
   }
-  pdl_wait();  // q' and the new token's cache entries come from the previous kernel
+  // batch 1 with the QKV records (deferred head epilogue): the RoPE factors of
+  // dims lane + 32 j at position p, loaded now (pos and the table are inputs
+  // of the step); the CTA of the last range, which holds position p, also
+  // forms the new token's key and value
+  const bool defer = a.qkv_part != nullptr;
+  const bool kv_task = defer && pos_ok && sp == NC - 1;
+  float2 rcs[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
+  if (defer) {
+    const int half = D / 2, pp = pos_ok ? p : 0;
+    rcs[0] = a.rope[(size_t)pp * half + lane];
+    if (half > 32) rcs[1] = a.rope[(size_t)pp * half + lane + 32];
+  }
+  pdl_wait();  // q' (or the QKV records) and the new token's cache entries come from the previous kernel
   bool ok = true;
+  const unsigned long long deadline = global_ns() + kWaitNs;
+  auto issue = [&](int slot, int i) {
+    const int c0 = (tile0 + i) * kTilePos;
+    const int n16 = (min(kTilePos, L - c0) + 15) & ~15;  // c0 + n16 <= round16(L) <= cap
+    if (!FUTR_DCHECK(c0 >= 0 && c0 + n16 <= cap, a.err)) return;  // debug build
+    const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
+    uint8_t* st = stages + (size_t)slot * Lay::kStage;
+    mbar_arrive_expect_tx(&full[slot], 2 * cb + 2 * sb);
+    bulk_g2s(st, strm + (size_t)c0 * (D / 2), cb, &full[slot]);
+    bulk_g2s(st + Lay::kCodes, strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), cb, &full[slot]);
+    bulk_g2s(st + 2 * Lay::kCodes, strm + (size_t)cap * D + 2 * (size_t)c0, sb, &full[slot]);
+    bulk_g2s(st + 2 * Lay::kCodes + 2 * kTilePos, strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb,
+             &full[slot]);
+  };
+  const int pre = ntiles < kAttnRing ? ntiles : kAttnRing;
+  if (warp == kAttnCW && lane == 0)
+    for (int i = 0; i < pre; ++i) issue(i, i);
+  float rn = 0.f;
+  if (defer) {
+    // every thread: the head tasks' sums (the first tiles are landing meanwhile)
+    sum_qkv_records<D>(a, b, hq0, Gv, kvh, kv_task, s_qs, &s_ss);
+    __syncthreads();
+    rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(s_ss, (float)a.hidden) + a.eps));
+  }
 
   if (warp == kAttnCW) {
     // ---------------------------------------------------------- producer --
+    if (kv_task) {
+      // the new token's key (RoPE, rotation) and value (rotation), INT4 with
+      // an fp16 scale each, for the consumer warp whose sub-tile holds it
+      float v[J];
+      int code[J];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        head_from_sums<D>(v, s_qs + (Gv + t) * D, rn, t == 0, rcs, a);
+        const __half sc = warp_quant<J>(v, code);
+#pragma unroll
+        for (int j = 0; j < J; ++j) s_tok[t][lane + 32 * j] = (int8_t)code[j];
+        if (lane == 0) s_toks[t] = sc;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_kvready);
+    }
     if (lane == 0) {
-      const unsigned long long deadline = global_ns() + kWaitNs;
-      auto issue = [&](int slot, int i) {
-        const int c0 = (tile0 + i) * kTilePos;
-        const int n16 = (min(kTilePos, L - c0) + 15) & ~15;  // c0 + n16 <= round16(L) <= cap
-        if (!FUTR_DCHECK(c0 >= 0 && c0 + n16 <= cap, a.err)) return;  // debug build
-        const uint32_t cb = (uint32_t)n16 * (D / 2), sb = (uint32_t)n16 * 2;
-        uint8_t* st = stages + (size_t)slot * Lay::kStage;
-        mbar_arrive_expect_tx(&full[slot], 2 * cb + 2 * sb);
-        bulk_g2s(st, strm + (size_t)c0 * (D / 2), cb, &full[slot]);
-        bulk_g2s(st + Lay::kCodes, strm + (size_t)cap * (D / 2) + (size_t)c0 * (D / 2), cb, &full[slot]);
-        bulk_g2s(st + 2 * Lay::kCodes, strm + (size_t)cap * D + 2 * (size_t)c0, sb, &full[slot]);
-        bulk_g2s(st + 2 * Lay::kCodes + 2 * kTilePos, strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb,
-                 &full[slot]);
-      };
-      const int pre = ntiles < kAttnRing ? ntiles : kAttnRing;
-      for (int i = 0; i < pre; ++i) issue(i, i);
       int slot = 0, issued = pre;
       uint32_t phase = 0;
       for (int i = kAttnRing; i < ntiles; ++i) {
@@ -177,17 +320,46 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
   } else {
     // ----------------------------------------------------------- consumers --
     // query fragments (B operand of K q'^T), once per CTA into shared memory
-    build_qfrag<D, NTQ>(a.qrot + ((size_t)b * a.Hq + hq0) * D, Gv, qf, tid, kAttnCW * 32);
+    if (defer) {
+      // the query heads' epilogue: q' in place of the sums; the first range
+      // also writes it to qrot
+      for (int i = warp; i < Gv; i += kAttnCW) {
+        float v[J];
+        head_from_sums<D>(v, s_qs + i * D, rn, true, rcs, a);
+        float* q = a.qrot + ((size_t)b * a.Hq + hq0 + i) * D;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          s_qs[i * D + lane + 32 * j] = v[j];
+          if (sp == 0) q[lane + 32 * j] = v[j];
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kAttnCW * 32) : "memory");  // consumers only
+      build_qfrag<D, NTQ, true>(s_qs, Gv, qf, tid, kAttnCW * 32);
+    } else {
+      build_qfrag<D, NTQ>(a.qrot + ((size_t)b * a.Hq + hq0) * D, Gv, qf, tid, kAttnCW * 32);
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(kAttnCW * 32) : "memory");  // consumers only
     AttnWarp<D, NTQ> aw;
     aw.init();
-    const unsigned long long deadline = global_ns() + kWaitNs;
     int slot = 0;
     uint32_t phase = 0;
     for (int i = 0; i < ntiles; ++i) {
       if (!mbar_wait_until(&full[slot], phase, deadline, a.err)) {
         ok = false;
         break;
+      }
+      const int c0 = (tile0 + i) * kTilePos;
+      if (kv_task && i == ntiles - 1 && warp == ((p - c0) >> 4)) {
+        // this warp's sub-tile holds the new token: its cache slot held no
+        // entry of this step when the tile was copied, so it is patched in
+        // the stage, then written to the cache for the later steps
+        if (!mbar_wait_until(&s_kvready, 0, deadline, a.err)) {
+          ok = false;
+          break;
+        }
+        patch_new_token<D>(stages + (size_t)slot * Lay::kStage, p - c0, p, s_tok, s_toks);
+        put_k_token<D>(strm, cap, p, s_tok[0], s_toks[0]);
+        put_v_token<D>(strm, cap, p, s_tok[1], s_toks[1]);
       }
       aw.tile(stages + (size_t)slot * Lay::kStage, min(kTilePos, L - (tile0 + i) * kTilePos), qf, a.qk_scale_log2);
       __syncwarp();
@@ -423,6 +595,7 @@ AttnPlan plan_attention(const futr_shape& s, int batch, int cap, int n_sm, int f
   if (nc > tiles) nc = tiles;
   if (nc < 1) nc = 1;
   p.NC = nc;
+  p.one_sub = attn_nsub(G) == 1;
   p.part_floats = 0;
   return p;
 }

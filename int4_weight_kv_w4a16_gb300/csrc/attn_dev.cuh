@@ -49,10 +49,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // shared memory qf[(ks * NTQ + nt) * 32 + lane]: column c of n-tile nt is head
 // slot (8 nt + c) mod 4 NTQ, its hi part (fp16 of the fp32 query) in the first
 // half of the columns, its lo part (fp16 of the remainder) in the second;
-// slots >= Gv are zero.  q: the sub-group's first query head [Gv][D] fp32
-// (read through L2: another CTA may have written it in this launch).  Items
-// first, first + stride, ...
-template <int D, int NTQ>
+// slots >= Gv are zero.  q: the sub-group's first query head [Gv][D] fp32,
+// in global memory (read through L2: another CTA may have written it in this
+// launch) or, with kShared, in this CTA's shared memory.  Items first, first +
+// stride, ...
+template <int D, int NTQ, bool kShared = false>
 __device__ __forceinline__ void build_qfrag(const float* q, int Gv, uint2* qf, int first, int stride) {
   for (int item = first; item < (D / 16) * NTQ * 32; item += stride) {
     const int ln = item & 31, ks = (item >> 5) / NTQ, nt = (item >> 5) - NTQ * ks;
@@ -60,8 +61,9 @@ __device__ __forceinline__ void build_qfrag(const float* q, int Gv, uint2* qf, i
     const int k0 = 16 * ks + 2 * (ln & 3);
     uint2 v = make_uint2(0u, 0u);
     if (hs < Gv) {
-      const float2 f0 = __ldcg(reinterpret_cast<const float2*>(q + hs * D + k0));
-      const float2 f1 = __ldcg(reinterpret_cast<const float2*>(q + hs * D + k0 + 8));
+      const float2* q2 = reinterpret_cast<const float2*>(q + hs * D + k0);
+      const float2 f0 = kShared ? q2[0] : __ldcg(q2);
+      const float2 f1 = kShared ? q2[4] : __ldcg(q2 + 4);
       uint32_t h0, l0q, h1, l1q;
       split_half2(f0.x, f0.y, h0, l0q);
       split_half2(f1.x, f1.y, h1, l1q);

@@ -418,65 +418,96 @@ struct KvView {
   }
 };
 
-// Write the codes (warp-held code[j] of dim lane+32j, codes in [-8,7]) and
-// scale of one token of one kv-head into slot p of a stream.  `scratch`:
-// per-warp shared buffer of d bytes.  K slots are plain stores of whole
-// words; V slots update the nibbles of position p only (an atomic AND then an
-// atomic OR per word), so other positions of the tile are left untouched.
-template <int J>
-__device__ __forceinline__ void store_k_token(uint8_t* strm, int cap, int p, const int (&code)[J],
-                                              __half s, int8_t* scratch) {
-  constexpr int d = 32 * J;
+// Key word w (< d/8) of one position: the 8 codes of dims 32 j + 2 t + {0, 8,
+// 16, 24, 1, 9, 17, 25} (t = w / (d/32), j = w % (d/32)) as nibbles code + 8.
+// codes: the position's d codes (int8, dim order).
+template <int d>
+__device__ __forceinline__ uint32_t k_token_word(const int8_t* codes, int w) {
+  const int t = w / (d / 32), j = w % (d / 32);
+  const int base = 32 * j + 2 * t;
+  const int dims[8] = {base, base + 8, base + 16, base + 24, base + 1, base + 9, base + 17, base + 25};
+  uint32_t v = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v |= (uint32_t)((codes[dims[i]] + 8) & 0xF) << (4 * i);
+  return v;
+}
+
+// Value word w (< 8 d/16) of the 16-position tile holding position p: its
+// word offset in the tile, the mask of position p's two nibbles in it and
+// their new bits (dims 16 j + gr and 16 j + 8 + gr; gr = w / (d/16), j = w %
+// (d/16)).
+struct VWord {
+  int off;
+  uint32_t mask, bits;
+};
+template <int d>
+__device__ __forceinline__ VWord v_token_word(const int8_t* codes, int p, int w) {
+  const int p16 = p & 15;
+  const int t = (p16 & 7) >> 1, hi = p16 >> 3, odd = p16 & 1;
+  const int sh = 16 * odd + 4 * hi;
+  const int gr = w / (d / 16), j = w % (d / 16);
+  const uint32_t n0 = (uint32_t)((codes[16 * j + gr] + 8) & 0xF);
+  const uint32_t n1 = (uint32_t)((codes[16 * j + 8 + gr] + 8) & 0xF);
+  return VWord{(4 * gr + t) * (d / 16) + j, (0xFu << sh) | (0xFu << (sh + 8)), (n0 << sh) | (n1 << (sh + 8))};
+}
+
+// Write one token of one kv-head into slot p of a stream (one warp): codes
+// (d int8 in [-8, 7], dim order, in shared memory) and scale.  K slots are
+// plain stores of whole words; V slots update the nibbles of position p only
+// (an atomic AND then an atomic OR per word), so other positions of the tile
+// are left untouched.
+template <int d>
+__device__ __forceinline__ void put_k_token(uint8_t* strm, int cap, int p, const int8_t* codes, __half s) {
   const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < J; ++j) scratch[lane + 32 * j] = (int8_t)code[j];
-  __syncwarp();
-  // d/8 words per position: lane index within position t = w / (d/32), word j = w % (d/32)
+  // d/8 words per position, contiguous
   if (lane < d / 8) {
-    const int t = lane / (d / 32), j = lane % (d / 32);
-    const int base = 32 * j + 2 * t;
-    const int dims[8] = {base, base + 8, base + 16, base + 24, base + 1, base + 9, base + 17, base + 25};
-    uint32_t w = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w |= (uint32_t)((scratch[dims[i]] + 8) & 0xF) << (4 * i);
     uint32_t* dst = reinterpret_cast<uint32_t*>(strm + (uint64_t)(p >> 3) * (4 * d) + (p & 7) * (d / 2));
-    dst[lane] = w;
+    dst[lane] = k_token_word<d>(codes, lane);
   }
   if (lane == 0) {
     __half* ks = reinterpret_cast<__half*>(strm + (uint64_t)cap * d);
     ks[p] = s;
   }
+}
+
+template <int d>
+__device__ __forceinline__ void put_v_token(uint8_t* strm, int cap, int p, const int8_t* codes, __half s) {
+  const int lane = threadIdx.x & 31;
+  uint32_t* tile = reinterpret_cast<uint32_t*>(strm + (uint64_t)cap * (d / 2) + (uint64_t)(p >> 4) * (8 * d));
+  for (int w = lane; w < 8 * (d / 16); w += 32) {
+    const VWord vw = v_token_word<d>(codes, p, w);
+    // clear, then set, the nibbles of position p: two reductions on the word
+    // (same thread, same address: applied in program order), no read back
+    atomicAnd(tile + vw.off, ~vw.mask);
+    atomicOr(tile + vw.off, vw.bits);
+  }
+  if (lane == 0) {
+    __half* vs = reinterpret_cast<__half*>(strm + (uint64_t)cap * d + 2ull * cap);
+    vs[p] = s;
+  }
+}
+
+// The same from warp-held codes (code[j] of dim lane + 32 j); `scratch`: a
+// per-warp shared buffer of d bytes.
+template <int J>
+__device__ __forceinline__ void store_k_token(uint8_t* strm, int cap, int p, const int (&code)[J],
+                                              __half s, int8_t* scratch) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < J; ++j) scratch[lane + 32 * j] = (int8_t)code[j];
+  __syncwarp();
+  put_k_token<32 * J>(strm, cap, p, scratch, s);
   __syncwarp();
 }
 
 template <int J>
 __device__ __forceinline__ void store_v_token(uint8_t* strm, int cap, int p, const int (&code)[J],
                                               __half s, int8_t* scratch) {
-  constexpr int d = 32 * J;
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < J; ++j) scratch[lane + 32 * j] = (int8_t)code[j];
   __syncwarp();
-  const int p16 = p & 15;
-  const int t = (p16 & 7) >> 1, hi = p16 >> 3, odd = p16 & 1;
-  const int sh = 16 * odd + 4 * hi;
-  uint32_t* tile = reinterpret_cast<uint32_t*>(strm + (uint64_t)cap * (d / 2) + (uint64_t)(p >> 4) * (8 * d));
-  // 8 lanes (gr = 0..7) x d/16 words
-  for (int w = lane; w < 8 * (d / 16); w += 32) {
-    const int gr = w / (d / 16), j = w % (d / 16);
-    const uint32_t n0 = (uint32_t)((scratch[16 * j + gr] + 8) & 0xF);
-    const uint32_t n1 = (uint32_t)((scratch[16 * j + 8 + gr] + 8) & 0xF);
-    uint32_t* dst = tile + (4 * gr + t) * (d / 16) + j;
-    const uint32_t mask = (0xFu << sh) | (0xFu << (sh + 8));
-    // clear, then set, the nibbles of position p: two reductions on the word
-    // (same thread, same address: applied in program order), no read back
-    atomicAnd(dst, ~mask);
-    atomicOr(dst, (n0 << sh) | (n1 << (sh + 8)));
-  }
-  if (lane == 0) {
-    __half* vs = reinterpret_cast<__half*>(strm + (uint64_t)cap * d + 2ull * cap);
-    vs[p] = s;
-  }
+  put_v_token<32 * J>(strm, cap, p, scratch, s);
   __syncwarp();
 }
 

@@ -243,6 +243,9 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
         }
       }
       publish_issued(flag, issued);
+      // QKV whose epilogue runs in the attention kernel: the blob header check
+      if (EPI == kEpiQkv && a.defer && blockIdx.x == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
+        set_err(a.err, FUTR_ERR_BAD_BLOB);
     } else {
       pdl_wait();
     }
@@ -264,7 +267,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
   // factors, loaded now and used by the epilogue (their latency hides under
   // the K-loop instead of lengthening the tail)
   HeadPre hp_pre{};
-  if (EPI == kEpiQkv && !kCluster) {
+  if (EPI == kEpiQkv && !kCluster && !a.defer) {
     const int hpr = kRowsPerBlock / a.d;
     if (warp < a.batch * hpr) hp_pre = head_pre(a, warp / hpr, rb * hpr + warp % hpr);
   }
@@ -505,6 +508,9 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
       }
       publish_issued(flag, issued);
+      // QKV whose epilogue runs in the attention kernel: the blob header check
+      if (EPI == kEpiQkv && a.defer && blockIdx.x == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
+        set_err(a.err, FUTR_ERR_BAD_BLOB);
     } else {
       pdl_wait();
     }

@@ -41,6 +41,9 @@ struct ProjArgs {
   __nv_bfloat16* out;
   int out_ld;
   // QKV
+  // 1: the CTAs only write their split records (every split, S > 1) and
+  // leave; the attention kernel adds them and runs the head epilogue (batch 1)
+  int defer;
   const uint64_t* blob_magic;
   float* qrot;                   // [batch][Hq][d] rotated query, fp32
   KvView kv;
@@ -65,7 +68,7 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
 cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream_t st, bool pdl);
 
 struct AttnArgs {
-  const float* qrot;             // [batch][Hq][d] rotated query, fp32
+  float* qrot;                   // [batch][Hq][d] rotated query, fp32 (written here with qkv_part)
   KvView kv;
   const int* pos;
   int batch, Hq, Hkv, G, nh;
@@ -73,10 +76,24 @@ struct AttnArgs {
   float had_c;
   __nv_bfloat16* out;            // [batch][Hq*d]
   int* err;
+  // The QKV projection's split records when it left its head epilogue to this
+  // kernel (ProjArgs::defer), else null: [row block][qkv_S][qkv_rec_floats]
+  // (row block stride qkv_stride records).  The CTAs then add the records of
+  // their query heads (and, in the CTA whose range holds the new position,
+  // of their kv-head's key and value rows), apply the RMSNorm factor, RoPE
+  // and the rotation, write q' to qrot (first range) and the new token's
+  // codes into the cache (last range).
+  const float* qkv_part;
+  int qkv_S, qkv_stride, qkv_rec_floats;
+  size_t qkv_part_cap;           // floats of qkv_part (debug-build bounds checks)
+  int hidden;                    // inputs of the QKV projection (RMSNorm mean)
+  float eps;
+  const float2* rope;            // [cap][d/2]
 };
 
 struct AttnPlan {
   int NC;                        // context ranges (cluster size) per (sequence, kv-head)
+  bool one_sub;                  // one head sub-group (one cluster) per kv-head and sequence
   size_t smem;
   size_t part_floats;            // global scratch (none: ranges merge in distributed shared memory)
 };
