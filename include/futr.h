@@ -252,8 +252,8 @@ futr_status futr_workspace_init(const futr_shape* shape, int32_t max_batch, int3
  * x, y: bf16 [batch][H] (may not alias).  pos: device int32 [batch], the number
  * of tokens already cached per sequence (sequence b uses cache slot b).
  * blob: packed weights of this layer.  Five kernels launched back to back with
- * programmatic dependent launch.  At batch 1 (when a kv-head has at most 8
- * query heads) the QKV kernel leaves its split-K partial sums in the workspace
+ * programmatic dependent launch.  When a kv-head has at most 8 query heads
+ * the QKV kernel leaves its split-K partial sums in the workspace
  * and the attention kernel adds them and runs the head epilogue (RMSNorm
  * factor, RoPE, rotation, the new token's quantization and placement);
  * FUTR_QKV_DEFER=0 keeps that epilogue in the QKV kernel.  Either way the
@@ -271,8 +271,8 @@ futr_status futr_decode_block(const uint16_t* x, const void* blob, const futr_kv
  * recorded before each kernel and after the last (without programmatic
  * overlap).  Synchronizes
  * `stream` and writes the five kernel times in milliseconds to
- * stage_ms_host[5] (QKV, attention, O, gate/up, down; at batch 1 the QKV head
- * epilogue counts in the attention time, see futr_decode_block). */
+ * stage_ms_host[5] (QKV, attention, O, gate/up, down; the QKV head epilogue
+ * counts in the attention time when it runs there, see futr_decode_block). */
 futr_status futr_decode_block_timed(const uint16_t* x, const void* blob, const futr_kv* kv,
                                     int32_t layer, int32_t batch, const int32_t* pos,
                                     uint16_t* y, const futr_ws* ws, void* stream,

@@ -95,29 +95,33 @@ struct Plans {
   ProjPlan proj[4];  // QKV, O, GU, DOWN
   AttnPlan attn;
   BlockPlan blk;     // the persistent whole-block kernel (batch <= 16)
-  // the five-kernel path at batch 1: QKV writes its split records only and
-  // the attention kernel adds them and runs the head epilogue
+  // the five kernels: QKV writes its split records only (kEpiQkvRec) and the
+  // attention kernel adds them and runs the head epilogue
   bool qkv_defer;
 };
+
+// Batches up to which the five kernels run the QKV head epilogue in the
+// attention kernel.
+constexpr int kQkvDeferMaxBatch = 32;
 
 Plans plan_all(const futr_shape& s, int batch, int cap, int n_sm, int force, int force_attn, bool allow_defer) {
   const BlobSections sec = blob_sections(s);
   Plans p;
   const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
-  for (int i = 0; i < 4; ++i)
-    p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force, epi[i]);
   p.attn = plan_attention(s, batch, cap, n_sm, force_attn);
+  // the QKV head epilogue in the attention kernel needs one cluster per
+  // kv-head and sequence (so one CTA forms each new token)
+  p.qkv_defer = allow_defer && batch <= kQkvDeferMaxBatch && p.attn.one_sub;
+  for (int i = 0; i < 4; ++i)
+    p.proj[i] = plan_projection(sec.rows[i], sec.cols[i], batch, n_sm, force,
+                                i == 0 && p.qkv_defer ? kEpiQkvRec : epi[i]);
   p.blk = batch <= kBlockMaxBatch ? plan_block(s, batch, cap, n_sm, 0) : BlockPlan{};
-  // one cluster per kv-head (so one CTA forms each new token) and records
-  // that exist (split QKV, global reduction)
-  const ProjPlan& q = p.proj[0];
-  p.qkv_defer = allow_defer && batch == 1 && p.attn.one_sub && !q.tc && !q.cluster && q.S > 1;
   return p;
 }
 
 // Launch plans of one decode call.  FUTR_SPLITK / FUTR_ATTN_SPLIT force the
 // split-K and context-range counts (within the planner's bounds);
-// FUTR_QKV_DEFER=0 keeps the QKV head epilogue in the QKV kernel at batch 1.
+// FUTR_QKV_DEFER=0 keeps the QKV head epilogue in the QKV kernel.
 // Plans are kept per (shape, batch, capacity, SM count, these settings), so a
 // repeated call only looks its plan up.
 Plans make_plans(const futr_shape& s, int batch, int cap, int n_sm) {
@@ -176,7 +180,8 @@ WsLayout ws_layout(const futr_shape& s, int max_batch, int cap, int n_sm) {
   for (int b = 1; b <= max_batch; ++b) {
     const Plans p = plan_all(s, b, cap, n_sm, 0, 0, true);
     for (int i = 0; i < 4; ++i)
-      if (p.proj[i].s_cap > 1 && p.proj[i].part_cap_floats > part) part = p.proj[i].part_cap_floats;
+      if ((p.proj[i].s_cap > 1 || p.proj[i].epi == kEpiQkvRec) && p.proj[i].part_cap_floats > part)
+        part = p.proj[i].part_cap_floats;
     if (p.attn.part_floats > apart) apart = p.attn.part_floats;
     if (b <= kBlockMaxBatch) {
       // the persistent kernel with the most CTAs any plan of this batch uses
@@ -421,12 +426,12 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
   }
 
   for (int i = 0; i < 4; ++i)
-    if (P.proj[i].S > 1 && P.proj[i].part_floats * 4 > ws->part_bytes) return FUTR_ERR_INVALID_ARG;
+    if ((P.proj[i].S > 1 || P.proj[i].epi == kEpiQkvRec) && P.proj[i].part_floats * 4 > ws->part_bytes)
+      return FUTR_ERR_INVALID_ARG;
   if (P.attn.part_floats * 4 > ws->apart_bytes) return FUTR_ERR_INVALID_ARG;
   if (P.qkv_defer) {
     // QKV leaves its records (in `part`, which O overwrites only after the
     // attention kernel has completed) to the attention kernel
-    PA[0].defer = 1;
     AT.qkv_part = part;
     AT.qkv_S = P.proj[0].S;
     AT.qkv_stride = P.proj[0].S;
@@ -436,14 +441,13 @@ futr_status run_block(const uint16_t* x, const void* blob, const futr_kv* kv, in
     AT.eps = s.rms_eps;
     AT.rope = PA[0].rope;
   }
-  const int epi[4] = {kEpiQkv, kEpiResid, kEpiSwiglu, kEpiResid};
   static const char* const names[4] = {"futr.qkv", "futr.o", "futr.gate_up", "futr.down"};
   cudaError_t e;
   for (int i = 0; i < 4; ++i) {
     if (events) cudaEventRecord(events[i == 0 ? 0 : i + 1], st);
     {
       Range r(names[i]);
-      e = launch_projection(epi[i], P.proj[i], PA[i], st, pdl);
+      e = launch_projection(P.proj[i].epi, P.proj[i], PA[i], st, pdl);
     }
     if (e != cudaSuccess) return FUTR_ERR_CUDA;
     if (i == 0) {

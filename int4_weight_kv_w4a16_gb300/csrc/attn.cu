@@ -35,8 +35,8 @@
 // until the leader is done.  No CTA leaves early, so every thread reaches
 // both barriers; the ring waits are bounded.
 //
-// At batch 1 the QKV projection leaves its split-K records (AttnArgs::qkv_part)
-// and the head epilogue runs here, after the wait: every CTA adds the records
+// By default the QKV projection leaves its split-K records
+// (AttnArgs::qkv_part) and the head epilogue runs here, after the wait: every CTA adds the records
 // of its query heads, applies the RMSNorm factor, RoPE and the rotation and
 // builds the query fragments from shared memory; in the CTA of the last range
 // the producer warp forms the new token's INT4 key and value, and the consumer
@@ -82,7 +82,7 @@ __device__ __forceinline__ float4 ld_dsmem4(const float4* local, uint32_t rank) 
   return v;
 }
 
-// ------------------------------------ QKV head epilogue (batch 1, deferred) --
+// ------------------------------------------ QKV head epilogue (deferred) --
 // The QKV projection left its split records (ProjArgs::defer).  Head task i of
 // this CTA: query head hq0 + i for i < Gv, then (kv) the key and the value
 // head of kv-head kvh.  qs[i * D + r] = the sum over the splits (in split
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
       l2_prefetch(strm + (size_t)cap * D + 2 * (size_t)cap + 2 * (size_t)c0, sb);
     }
   }
-  // batch 1 with the QKV records (deferred head epilogue): the RoPE factors of
+  // with the QKV records (deferred head epilogue): the RoPE factors of
   // dims lane + 32 j at position p, loaded now (pos and the table are inputs
   // of the step); the CTA of the last range, which holds position p, also
   // forms the new token's key and value

@@ -167,7 +167,7 @@ __device__ __forceinline__ void cluster_epilogue(const ProjArgs& a, const float*
 // the row block.
 template <int NTP, int EPI>
 constexpr bool cluster_reduce() {
-  return NTP != 0 && EPI != kEpiSwiglu;
+  return NTP != 0 && EPI != kEpiSwiglu && EPI != kEpiQkvRec;
 }
 
 // NTP: batch tiles of 8 columns, 1..4; 0 = one batch row (one tile, the
@@ -244,7 +244,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
       }
       publish_issued(flag, issued);
       // QKV whose epilogue runs in the attention kernel: the blob header check
-      if (EPI == kEpiQkv && a.defer && blockIdx.x == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
+      if (EPI == kEpiQkvRec && blockIdx.x == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
         set_err(a.err, FUTR_ERR_BAD_BLOB);
     } else {
       pdl_wait();
@@ -267,7 +267,7 @@ __device__ __forceinline__ void proj_body(const ProjArgs& a, const CUtensorMap* 
   // factors, loaded now and used by the epilogue (their latency hides under
   // the K-loop instead of lengthening the tail)
   HeadPre hp_pre{};
-  if (EPI == kEpiQkv && !kCluster && !a.defer) {
+  if (EPI == kEpiQkv && !kCluster) {
     const int hpr = kRowsPerBlock / a.d;
     if (warp < a.batch * hpr) hp_pre = head_pre(a, warp / hpr, rb * hpr + warp % hpr);
   }
@@ -508,9 +508,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         }
       }
       publish_issued(flag, issued);
-      // QKV whose epilogue runs in the attention kernel: the blob header check
-      if (EPI == kEpiQkv && a.defer && blockIdx.x == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
-        set_err(a.err, FUTR_ERR_BAD_BLOB);
     } else {
       pdl_wait();
     }
@@ -844,6 +841,7 @@ int resident_ctas(int nt, int epi, size_t smem) {
   FUTR_OCC(0, 0) FUTR_OCC(1, 0) FUTR_OCC(2, 0) FUTR_OCC(3, 0) FUTR_OCC(4, 0)
   FUTR_OCC(0, 1) FUTR_OCC(1, 1) FUTR_OCC(2, 1) FUTR_OCC(3, 1) FUTR_OCC(4, 1)
   FUTR_OCC(0, 2) FUTR_OCC(1, 2) FUTR_OCC(2, 2) FUTR_OCC(3, 2) FUTR_OCC(4, 2)
+  FUTR_OCC(0, 3) FUTR_OCC(1, 3) FUTR_OCC(2, 3) FUTR_OCC(3, 3) FUTR_OCC(4, 3)
 #undef FUTR_OCC
   return e == cudaSuccess ? n : 0;
   });
@@ -966,8 +964,9 @@ ProjPlan plan_projection(int rows, int cols, int batch, int n_sm, int force_spli
   // placed more slowly than single CTAs while the previous kernel still holds
   // SM slots, which costs more than the shorter tail saves (8B: 52.8 vs 62.4
   // µs), and gate/up (hundreds of row blocks, a short SwiGLU tail) lost 2-6 µs
-  // to whole-cluster waves: both keep the global records.
-  p.cluster = !p.tc && batch > 1 && epi != kEpiSwiglu;
+  // to whole-cluster waves: both keep the global records.  The records-only
+  // QKV (kEpiQkvRec) has no epilogue here and writes global records too.
+  p.cluster = !p.tc && batch > 1 && epi != kEpiSwiglu && epi != kEpiQkvRec;
   const int fit = p.tc ? resident_tc(epi, p.smem) : resident_ctas(batch == 1 ? 0 : p.nt, epi, p.smem);
   const int s_max =
       p.cluster ? std::min({p.s_cap, kMaxProjCluster, max_proj_cluster(batch == 1 ? 0 : p.nt, epi, p.smem)}) : p.s_cap;
@@ -1015,6 +1014,7 @@ cudaError_t launch_projection(int epi, const ProjPlan& p, ProjArgs a, cudaStream
   }
   if (epi == kEpiResid) return launch_nt<kEpiResid>(p.nt, a, grid, p.smem, st, pdl);
   if (epi == kEpiSwiglu) return launch_nt<kEpiSwiglu>(p.nt, a, grid, p.smem, st, pdl);
+  if (epi == kEpiQkvRec) return launch_nt<kEpiQkvRec>(p.nt, a, grid, p.smem, st, pdl);
   return launch_nt<kEpiQkv>(p.nt, a, grid, p.smem, st, pdl);
 }
 

@@ -17,6 +17,9 @@ constexpr int kProjMaxSmem = 200 * 1024;
 constexpr int kEpiResid = 0;
 constexpr int kEpiSwiglu = 1;
 constexpr int kEpiQkv = 2;
+// QKV whose CTAs only write their split records (with the sums of squares)
+// and leave: the attention kernel adds them and runs the head epilogue
+constexpr int kEpiQkvRec = 3;
 
 struct ProjArgs {
   const uint8_t* w;              // section base of the packed blob
@@ -41,9 +44,6 @@ struct ProjArgs {
   __nv_bfloat16* out;
   int out_ld;
   // QKV
-  // 1: the CTAs only write their split records (every split, S > 1) and
-  // leave; the attention kernel adds them and runs the head epilogue (batch 1)
-  int defer;
   const uint64_t* blob_magic;
   float* qrot;                   // [batch][Hq][d] rotated query, fp32
   KvView kv;
@@ -77,7 +77,7 @@ struct AttnArgs {
   __nv_bfloat16* out;            // [batch][Hq*d]
   int* err;
   // The QKV projection's split records when it left its head epilogue to this
-  // kernel (ProjArgs::defer), else null: [row block][qkv_S][qkv_rec_floats]
+  // kernel (kEpiQkvRec), else null: [row block][qkv_S][qkv_rec_floats]
   // (row block stride qkv_stride records).  The CTAs then add the records of
   // their query heads (and, in the CTA whose range holds the new position,
   // of their kv-head's key and value rows), apply the RMSNorm factor, RoPE

@@ -227,7 +227,7 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
     flag[1] = 1;
   }
   // debug build: this CTA's split record and row block lie inside their regions
-  if (tid == 0 && (S > 1 || (EPI == kEpiQkv && a.defer)) &&
+  if (tid == 0 && (S > 1 || EPI == kEpiQkvRec) &&
       !FUTR_DCHECK(rb < a.n_rb && slot < a.part_stride &&
                        ((size_t)rb * a.part_stride + a.part_stride) * a.rec_floats <= a.part_cap,
                    a.err))
@@ -240,10 +240,10 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
   write_red(red);
   consumer_sync();
 
-  // QKV at batch 1: the record is all this kernel writes (the attention
+  // records-only QKV: the record is all this kernel writes (the attention
   // kernel adds the records and runs the head epilogue)
-  const bool defer = EPI == kEpiQkv && a.defer;
-  if (S > 1 || defer) {
+  constexpr bool kDefer = EPI == kEpiQkvRec;
+  if (S > 1 || kDefer) {
     // publish this split's partial record: per batch row 32 float4 of sums and
     // one float4 (sum of squares, 0, 0, 0); then count arrivals
     float* rec = a.part + ((size_t)rb * a.part_stride + slot) * a.rec_floats;
@@ -254,7 +254,7 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
                                : make_float4(EPI != kEpiResid ? ss[n] : 0.f, 0.f, 0.f, 0.f);
       reinterpret_cast<float4*>(rec + n * kRecLd)[c4] = v;
     }
-    if (defer) return;  // (the producer of CTA 0 checks the blob header)
+    if (kDefer) return;  // (the producer of CTA 0 checks the blob header)
     consumer_sync();
     if (tid == 0)
       flag[0] = atom_add_acq_rel_gpu(&a.cnt[rb], 1u) == (unsigned)(S - 1) ? 1 : 0;
@@ -374,7 +374,7 @@ __device__ __forceinline__ void proj_tail(const ProjArgs& a, float* red, int rb,
       const size_t o = (size_t)n * a.out_ld + (size_t)rb * 64 + r;
       if (FUTR_DCHECK(o < a.out_cap, a.err)) a.out[o] = __float2bfloat16_rn(sg * u);
     }
-  } else {
+  } else if (EPI == kEpiQkv) {
     if (rb == 0 && tid == 0 && a.blob_magic && *a.blob_magic != kBlobMagic)
       set_err(a.err, FUTR_ERR_BAD_BLOB);
     const int hpr = kRowsPerBlock / a.d;

@@ -215,9 +215,9 @@ def test_decode_8b_b1_ctx1024(monkeypatch, defer):
     run_case(wl.shape, wl.batch, inputs.context_lengths(wl))
 
 
-# Batch 1: the QKV kernel leaves its split records and the attention kernel
-# runs the head epilogue, the CTA of the last context range forming the new
-# token and patching it into its ring stage.  The new position at the first,
+# The QKV kernel leaves its split records and the attention kernel runs the
+# head epilogue, the CTA of the last context range forming the new token and
+# patching it into its ring stage.  The new position at the first,
 # middle and last slot of a 16-position sub-tile and of a 64-position tile
 # (each of the four consumer warps patches once), and past one tile.
 @pytest.mark.parametrize("length", [0, 15, 16, 47, 63, 64, 130])
@@ -225,9 +225,9 @@ def test_decode_b1_new_token_positions(length):
     run_case(TOY, 1, [length], seed=200 + length)
 
 
-# The head epilogue in either kernel at batch 1, head dims 64 and 128, one to
-# six query heads per cluster (one or two query n-tiles); with 12 heads per
-# kv-head (two sub-groups) it stays in the QKV kernel either way.
+# The head epilogue in either kernel, head dims 64 and 128, one to six query
+# heads per cluster (one or two query n-tiles); with 12 heads per kv-head (two
+# sub-groups) it stays in the QKV kernel either way.
 @pytest.mark.parametrize("name", ["g1", "g3", "g6_d128", "g12"])
 @pytest.mark.parametrize("defer", ["1", "0"], ids=["epilogue_in_attention", "epilogue_in_qkv"])
 def test_decode_b1_qkv_epilogue_placement(monkeypatch, name, defer):
@@ -235,7 +235,19 @@ def test_decode_b1_qkv_epilogue_placement(monkeypatch, name, defer):
     run_case(GROUP_SHAPES[name], 1, [77], seed=21)
 
 
-def test_decode_8b_b8_ctx1024():
+# The QKV kernel's own epilogue from batch 2 on (the split-K cluster reduction,
+# one, two and four batch tiles), which the records-only kernel replaces by
+# default.
+@pytest.mark.parametrize("batch", [2, 9, 32])
+def test_decode_qkv_epilogue_in_qkv_kernel(monkeypatch, batch):
+    monkeypatch.setenv("FUTR_QKV_DEFER", "0")
+    r = np.random.default_rng(300 + batch)
+    run_case(TOY, batch, list(r.integers(0, 200, size=batch)), seed=300 + batch)
+
+
+@pytest.mark.parametrize("defer", ["1", "0"], ids=["epilogue_in_attention", "epilogue_in_qkv"])
+def test_decode_8b_b8_ctx1024(monkeypatch, defer):
+    monkeypatch.setenv("FUTR_QKV_DEFER", defer)
     wl = WORKLOADS["llama8b_b8_ctx1024"]
     run_case(wl.shape, wl.batch, inputs.context_lengths(wl))
 
