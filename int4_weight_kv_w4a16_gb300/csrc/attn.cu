@@ -83,7 +83,7 @@ __device__ __forceinline__ float4 ld_dsmem4(const float4* local, uint32_t rank) 
 }
 
 // ------------------------------------------ QKV head epilogue (deferred) --
-// The QKV projection left its split records (ProjArgs::defer).  Head task i of
+// The QKV projection left its split records (kEpiQkvRec).  Head task i of
 // this CTA: query head hq0 + i for i < Gv, then (kv) the key and the value
 // head of kv-head kvh.  qs[i * D + r] = the sum over the splits (in split
 // order) of row r of task i's head, batch row b; *ss = the sum of squares of
