@@ -221,7 +221,9 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
     s_timeout = 0;
   }
   __syncthreads();
-  pdl_trigger();
+  // the next kernel may launch now; with the QKV records, only once they are
+  // summed (its CTAs' weight prefetch would compete with these L2 loads)
+  if (a.qkv_part == nullptr) pdl_trigger();
   // pos is an input of the step (the previous kernel does not write it), so the
   // range is known before the wait; the first tiles are pulled into L2 now
   // (a prefetch cannot return stale data: the copies after the wait read
@@ -279,6 +281,7 @@ __global__ void __launch_bounds__(kAttnThreads, NTQ == 1 ? 4 : 3) attn_kernel(co
     // every thread: the head tasks' sums (the first tiles are landing meanwhile)
     sum_qkv_records<D>(a, b, hq0, Gv, kvh, kv_task, s_qs, &s_ss);
     __syncthreads();
+    pdl_trigger();
     rn = __fdiv_rn(1.0f, sqrtf(__fdiv_rn(s_ss, (float)a.hidden) + a.eps));
   }
 
