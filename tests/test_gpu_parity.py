@@ -490,6 +490,12 @@ def test_workspace_size_ignores_forced_splits(monkeypatch):
         monkeypatch.setenv("FUTR_ATTN_SPLIT", v)
         assert {b: futr.futr_workspace_size(cs, b, 4096) for b in (1, 8, 32)} == base
         assert_close(bits_to_f64(gpu.decode(x, pos)), ref, f"forced splits {v}", rel=2e-3)
+    # nor does keeping the QKV epilogue in the QKV kernel
+    monkeypatch.delenv("FUTR_SPLITK")
+    monkeypatch.delenv("FUTR_ATTN_SPLIT")
+    monkeypatch.setenv("FUTR_QKV_DEFER", "0")
+    assert {b: futr.futr_workspace_size(cs, b, 4096) for b in (1, 8, 32)} == base
+    assert_close(bits_to_f64(gpu.decode(x, pos)), ref, "QKV epilogue in the QKV kernel", rel=2e-3)
 
 
 @pytest.mark.parametrize("persistent", ["1", "0"], ids=["whole_block", "five_kernels"])
