@@ -38,7 +38,11 @@ def assert_close(got: np.ndarray, ref: np.ndarray, name: str, rel=REL_L2, mx=MAX
     """rel L2 <= rel and |got - ref| <= mx * rms(ref) elementwise.  flip=True
     (stage checks of bf16 outputs) also allows each element one bf16 step at
     the larger of |got| and |ref|: a value that lands within the kernel's fp32
-    error of a rounding boundary may round the other way."""
+    error of a rounding boundary may round the other way.  Such a flip of one
+    large element can exceed the L2 bound of a small output by itself (one
+    flip in 512 values: ~3.5e-4), so with flip=True the L2 bound may instead
+    hold over the other elements while the one-step differences number at
+    most max(4, n / 2000), the end-to-end check's allowance for ties."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
@@ -49,7 +53,15 @@ def assert_close(got: np.ndarray, ref: np.ndarray, name: str, rel=REL_L2, mx=MAX
     if nrm == 0:
         assert np.abs(got).max() == 0, name
         return {"rel_l2": 0.0, "max_abs_rms": 0.0}
-    assert err / nrm <= rel, f"{name}: rel L2 {err / nrm:.3e} > {rel}"
+    if flip and err / nrm > rel:
+        step = bf16_ulp(np.maximum(np.abs(ref), np.abs(got))) * (1 + 1e-12)
+        one = (got != ref) & (np.abs(got - ref) <= step)
+        n_one = int(one.sum())
+        rest = np.linalg.norm(np.where(one, 0.0, got - ref))
+        assert n_one <= max(4, got.size // 2000) and rest / nrm <= rel, \
+            f"{name}: rel L2 {err / nrm:.3e} > {rel} ({n_one} one-step differences, rest {rest / nrm:.3e})"
+    else:
+        assert err / nrm <= rel, f"{name}: rel L2 {err / nrm:.3e} > {rel}"
     allowed = mx * rms
     if flip:
         allowed = np.maximum(allowed, bf16_ulp(np.maximum(np.abs(ref), np.abs(got))) * (1 + 1e-12))

@@ -245,6 +245,26 @@ def test_decode_qkv_epilogue_in_qkv_kernel(monkeypatch, batch):
     run_case(TOY, batch, list(r.integers(0, 200, size=batch)), seed=300 + batch)
 
 
+# Batch 1 at head_dim 128 with 2 to 4 query heads per kv-head (one n-tile of
+# hi|lo query columns), one and two kv-heads, one and two context ranges: the
+# new position in the first tile, at its last slot, at the next tile's first,
+# and past two tiles (the last range then holds one or two tiles).
+D128_SHAPES = {
+    "h1g4": dataclasses.replace(TOY, n_q_heads=4, n_kv_heads=1, head_dim=128, had_block=128),
+    "h2g4": dataclasses.replace(TOY, n_q_heads=8, n_kv_heads=2, head_dim=128, had_block=128),
+    "h2g3": dataclasses.replace(TOY, n_q_heads=6, n_kv_heads=2, head_dim=128, had_block=128),
+    "h2g2": dataclasses.replace(TOY, n_q_heads=4, n_kv_heads=2, head_dim=128, had_block=128),
+}
+
+
+@pytest.mark.parametrize("name", list(D128_SHAPES))
+@pytest.mark.parametrize("ranges", ["1", "2"])
+@pytest.mark.parametrize("length", [0, 63, 64, 130])
+def test_decode_b1_d128_query_groups(monkeypatch, name, ranges, length):
+    monkeypatch.setenv("FUTR_ATTN_SPLIT", ranges)
+    run_case(D128_SHAPES[name], 1, [length], seed=31 + length)
+
+
 @pytest.mark.parametrize("defer", ["1", "0"], ids=["epilogue_in_attention", "epilogue_in_qkv"])
 def test_decode_8b_b8_ctx1024(monkeypatch, defer):
     monkeypatch.setenv("FUTR_QKV_DEFER", defer)
